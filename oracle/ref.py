@@ -1,0 +1,170 @@
+"""CPU oracle for chunk-aligned window softmax attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline / reference arm may import this
+module. The CUDA library never does, and this module imports nothing from it: the two share no code. It is
+plain, slow and written to be checked by eye, in float64.
+
+What is computed (the VDN-Minimax-H3 window-attention article, lqnn.cn):
+  * section 一 (why window attention): the packed sequence holds T latent frames of S spatial tokens each plus G
+    global text/audio tokens. Frames are grouped into chunks of K latent frames; a query of frame t, in chunk
+    c = floor(t / K), may see only the whole chunks in [c - radius, c + radius]; the global tokens stay fully
+    connected (every query sees them, and a global query sees every token).
+  * section 三 (the decomposed idea): the result is mathematically identical to the masked kernel: each query's
+    softmax is normalised over exactly its kept set; the article keeps an eager per-frame loop as the
+    correctness baseline, which is the shape of ``window_attention`` below.
+Readings where the article is silent (each one is listed with its reason in the design notes):
+  * chunks past either end of the sequence do not exist: the window is clamped, not shifted;
+  * T need not be a multiple of K: the last chunk is partial and otherwise ordinary;
+  * globals sit after the frame tokens (global_pos = 0) or before them (global_pos = 1);
+  * scores are scaled by 1/sqrt(D); non-causal; no bias, softcap or dropout.
+
+Every function here is pinned by tests/test_oracle.py against facts that do not come from this file
+(brute force over an explicit mask, a library dense-attention routine in the special cases that reduce to it,
+closed forms and invariants), so no function is "parity unpinned".
+"""
+import math
+
+import numpy as np
+
+
+# ----------------------------------------------------------------------------------------------- geometry
+def num_chunks(T, K):
+    """Number of chunks: ceil(T / K) (the last chunk may hold fewer than K frames)."""
+    return (T + K - 1) // K
+
+
+def frame_offset(G, global_pos):
+    """Index of the first frame token: 0 when the globals come after the frames, G when they come first."""
+    return G if global_pos else 0
+
+
+def global_offset(T, S, global_pos):
+    """Index of the first global token: T*S when the globals come after the frames, 0 when they come first."""
+    return 0 if global_pos else T * S
+
+
+def frame_rows(t, S, f0):
+    """Sequence indices of the S tokens of latent frame t (frame-major packing, section 一)."""
+    return np.arange(f0 + t * S, f0 + (t + 1) * S, dtype=np.int64)
+
+
+def window_chunks(c, r, nc):
+    """Chunks visible from chunk c: the chunks of [c - r, c + r] that exist (section 一, window_bounds)."""
+    return list(range(max(0, c - r), min(nc - 1, c + r) + 1))
+
+
+def kept_set_of_frame(t, T, S, K, r, G, global_pos):
+    """Sorted sequence indices a query token of frame t attends to: its window's frames plus all globals."""
+    nc = num_chunks(T, K)
+    f0 = frame_offset(G, global_pos)
+    g0 = global_offset(T, S, global_pos)
+    c = t // K
+    idx = []
+    for cc in window_chunks(c, r, nc):
+        for tt in range(cc * K, min(T, (cc + 1) * K)):
+            idx.append(frame_rows(tt, S, f0))
+    idx.append(np.arange(g0, g0 + G, dtype=np.int64))
+    return np.sort(np.concatenate(idx))
+
+
+def kept_set_of_global(T, S, G):
+    """A global query attends to the whole packed sequence (section 一: globals stay fully connected)."""
+    return np.arange(T * S + G, dtype=np.int64)
+
+
+# ------------------------------------------------------------------------------------------------ softmax
+def attend(q_rows, k_kept, v_kept, scale):
+    """Plain attention of some query rows over one kept set, float64.
+
+    q_rows [n, D], k_kept / v_kept [m, D]. Scores s = q.k * scale; p = exp(s - max s) / sum exp(.) over the kept
+    set only; out = p @ v. Returns (out [n, D], p [n, m]).
+    """
+    s = (q_rows @ k_kept.T) * scale
+    s = s - s.max(axis=1, keepdims=True)
+    e = np.exp(s)
+    p = e / e.sum(axis=1, keepdims=True)
+    return p @ v_kept, p
+
+
+def _as64(x):
+    if hasattr(x, "detach"):  # a torch tensor: upcast through float32 (exact for bf16)
+        x = x.detach().float().cpu().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def window_attention(q, k, v, T, S, K, r, G, global_pos, return_probs=False):
+    """Chunk-aligned window softmax attention over a packed sequence, by an eager per-frame loop.
+
+    q, k, v: [B, L, H, D] with L = T*S + G (numpy or torch; upcast to float64 from the same values the GPU sees).
+    Returns out [B, L, H, D] float64. With ``return_probs`` it also returns a dict mapping (b, h, row) to
+    (kept indices, probabilities) for every row (debug mode; tiny inputs only).
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, L, H, D = q.shape
+    assert L == T * S + G, "sequence length must be T*S + G"
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros_like(q)
+    probs = {} if return_probs else None
+    f0 = frame_offset(G, global_pos)
+    g0 = global_offset(T, S, global_pos)
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                kept = kept_set_of_frame(t, T, S, K, r, G, global_pos)
+                rows = frame_rows(t, S, f0)
+                o, p = attend(q[b, rows, h], k[b, kept, h], v[b, kept, h], scale)
+                out[b, rows, h] = o
+                if return_probs:
+                    for i, row in enumerate(rows):
+                        probs[(b, h, int(row))] = (kept, p[i])
+            if G:
+                kept = kept_set_of_global(T, S, G)
+                rows = np.arange(g0, g0 + G, dtype=np.int64)
+                o, p = attend(q[b, rows, h], k[b, kept, h], v[b, kept, h], scale)
+                out[b, rows, h] = o
+                if return_probs:
+                    for i, row in enumerate(rows):
+                        probs[(b, h, int(row))] = (kept, p[i])
+    return (out, probs) if return_probs else out
+
+
+def window_attention_rows(q, k, v, T, S, K, r, G, global_pos, b, h, frames=(), global_rows=False):
+    """The same computation restricted to one (b, h) slice and to the listed frames (and the global rows).
+
+    Rows are independent, so each returned row equals the matching row of ``window_attention``. Returns a dict
+    {row index: output row (float64 [D])}. Used to check large workloads on a sample of rows.
+    """
+    D = q.shape[-1]
+    scale = 1.0 / math.sqrt(D)
+    f0 = frame_offset(G, global_pos)
+    g0 = global_offset(T, S, global_pos)
+    res = {}
+    for t in frames:
+        kept = kept_set_of_frame(t, T, S, K, r, G, global_pos)
+        rows = frame_rows(t, S, f0)
+        o, _ = attend(_as64(q[b, rows, h]), _as64(k[b, kept, h]), _as64(v[b, kept, h]), scale)
+        for i, row in enumerate(rows):
+            res[int(row)] = o[i]
+    if global_rows and G:
+        kept = kept_set_of_global(T, S, G)
+        rows = np.arange(g0, g0 + G, dtype=np.int64)
+        kk, vv = _as64(k[b, kept, h]), _as64(v[b, kept, h])
+        for lo in range(0, G, 256):  # bounded score blocks: G x L may not fit in memory at once
+            sel = rows[lo:lo + 256]
+            o, _ = attend(_as64(q[b, sel, h]), kk, vv, scale)
+            for i, row in enumerate(sel):
+                res[int(row)] = o[i]
+    return res
+
+
+def chunk_frames(c, T, K):
+    """Latent frames of chunk c."""
+    return list(range(c * K, min(T, (c + 1) * K)))
+
+
+def kept_pairs(T, S, K, r, G, global_pos=0):
+    """Number of kept (query, key) pairs of one (b, h) slice, counted from the kept sets themselves."""
+    n = 0
+    for t in range(T):
+        n += S * len(kept_set_of_frame(t, T, S, K, r, G, global_pos))
+    return n + G * (T * S + G)
