@@ -1,0 +1,221 @@
+"""chunk_windowed_softmax_gb300: chunk-aligned window softmax attention on GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/wa.h`` (``libwa.so``, built in-tree by ``_build.build()``).
+Functions keep the C names; this module only marshals arguments: every step of the computation runs in the
+library's CUDA kernels. PyTorch supplies device memory and streams. There is no CPU fallback: if the library
+is missing or a call fails, an exception is raised.
+"""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libwa.so")
+
+WA_OK = 0
+STATUS = {0: "WA_OK", 1: "WA_ERR_INVALID", 2: "WA_ERR_UNSUPPORTED", 3: "WA_ERR_OOM", 4: "WA_ERR_CUDA",
+          5: "WA_ERR_DEVICE_TIMEOUT", 6: "WA_ERR_DEVICE_BOUNDS"}
+
+# Symbols declared in include/wa.h (the tests check that the library exports each of them).
+EXPORTS = ("wa_plan_create", "wa_forward", "wa_plan_check_error", "wa_plan_info", "wa_plan_release",
+           "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount")
+
+
+class WAError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+class wa_layout_t(ctypes.Structure):
+    _fields_ = [("global_pos", ctypes.c_int32), ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("stride_b", ctypes.c_int64), ("stride_l", ctypes.c_int64), ("stride_h", ctypes.c_int64)]
+
+
+class wa_plan_info_t(ctypes.Structure):
+    _fields_ = [("n_chunks", ctypes.c_int32), ("n_groups", ctypes.c_int32), ("n_splits", ctypes.c_int32),
+                ("n_items", ctypes.c_int32), ("L", ctypes.c_int64), ("kept_pairs", ctypes.c_int64),
+                ("window_pairs", ctypes.c_int64), ("global_pairs", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64), ("kv_tiles", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class wa_group_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("q_lo", "q_hi", "kv0_lo", "kv0_hi", "kv1_lo", "kv1_hi")]
+
+
+_lib_handle = None
+
+
+def lib():
+    """Load libwa.so (once). Raises if it has not been built: there is no fallback."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                               f"g.build()'` (nvcc, sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        L.wa_plan_create.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(wa_layout_t), ctypes.POINTER(P)]
+        L.wa_plan_create.restype = ctypes.c_int
+        L.wa_forward.argtypes = [P, P, P, P, P, P]
+        L.wa_forward.restype = ctypes.c_int
+        L.wa_plan_check_error.argtypes = [P, P]
+        L.wa_plan_check_error.restype = ctypes.c_int
+        L.wa_plan_info.argtypes = [P, ctypes.POINTER(wa_plan_info_t)]
+        L.wa_plan_info.restype = ctypes.c_int
+        L.wa_plan_release.argtypes = [P]
+        L.wa_plan_release.restype = None
+        L.wa_geometry_describe.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(wa_layout_t),
+                                                                 ctypes.POINTER(wa_plan_info_t),
+                                                                 ctypes.POINTER(wa_group_t), ctypes.c_int64,
+                                                                 ctypes.POINTER(ctypes.c_int64), ctypes.c_int64]
+        L.wa_geometry_describe.restype = ctypes.c_int
+        L.wa_status_string.argtypes = [ctypes.c_int]
+        L.wa_status_string.restype = ctypes.c_char_p
+        L.wa_plan_set_debug_flags.argtypes = [P, ctypes.c_int]
+        L.wa_plan_set_debug_flags.restype = ctypes.c_int
+        L.wa_cache_size.argtypes = []
+        L.wa_cache_size.restype = ctypes.c_int
+        L.wa_plan_refcount.argtypes = [P]
+        L.wa_plan_refcount.restype = ctypes.c_int
+        _lib_handle = L
+    return _lib_handle
+
+
+def _check(st, what):
+    if st != WA_OK:
+        raise WAError(st, what)
+
+
+def make_layout(B, L, H, D, global_pos, strides=None):
+    """Layout of a [B, L, H, D] tensor; `strides` are element strides (b, l, h), contiguous by default."""
+    if strides is None:
+        strides = (L * H * D, H * D, D)
+    return wa_layout_t(global_pos, B, H, D, *strides)
+
+
+# ------------------------------------------------------------------------------------- C-named wrappers
+def wa_status_string(status):
+    return lib().wa_status_string(status).decode()
+
+
+def wa_plan_create(T, S, K, r, G, layout):
+    """Returns a plan handle (ctypes.c_void_p); raises WAError on failure."""
+    h = ctypes.c_void_p()
+    _check(lib().wa_plan_create(T, S, K, r, G, ctypes.byref(layout), ctypes.byref(h)), "wa_plan_create")
+    return h
+
+
+def wa_forward(plan, q_ptr, k_ptr, v_ptr, out_ptr, stream_ptr):
+    _check(lib().wa_forward(plan, ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                            ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream_ptr)), "wa_forward")
+
+
+def wa_plan_check_error(plan, stream_ptr):
+    return lib().wa_plan_check_error(plan, ctypes.c_void_p(stream_ptr))
+
+
+def wa_plan_info(plan):
+    info = wa_plan_info_t()
+    _check(lib().wa_plan_info(plan, ctypes.byref(info)), "wa_plan_info")
+    return info.as_dict()
+
+
+def wa_plan_release(plan):
+    lib().wa_plan_release(plan)
+
+
+def wa_geometry_describe(T, S, K, r, G, layout, with_groups=True, with_items=False):
+    """Host-only plan description: (info dict, list of group dicts, list of item tuples)."""
+    L = lib()
+    info = wa_plan_info_t()
+    _check(L.wa_geometry_describe(T, S, K, r, G, ctypes.byref(layout), ctypes.byref(info), None, 0, None, 0),
+           "wa_geometry_describe")
+    groups, items = [], []
+    gbuf = (wa_group_t * max(1, info.n_groups))() if with_groups else None
+    ibuf = (ctypes.c_int64 * (8 * max(1, info.n_items)))() if with_items else None
+    _check(L.wa_geometry_describe(T, S, K, r, G, ctypes.byref(layout), ctypes.byref(info), gbuf, info.n_groups,
+                                  ibuf, info.n_items), "wa_geometry_describe")
+    if with_groups:
+        groups = [{n: getattr(g, n) for n, _ in wa_group_t._fields_} for g in gbuf[:info.n_groups]]
+    if with_items:
+        items = [tuple(ibuf[8 * i:8 * i + 8]) for i in range(info.n_items)]
+    return info.as_dict(), groups, items
+
+
+# ----------------------------------------------------------------------------------------- torch side
+class Plan:
+    """A referenced plan for one geometry and layout on the current CUDA device."""
+
+    def __init__(self, T, S, K, r, G, B, H, D, global_pos=0, strides=None):
+        self.geometry = (T, S, K, r, G)
+        self.L = T * S + G
+        self.layout = make_layout(B, self.L, H, D, global_pos, strides)
+        self.handle = wa_plan_create(T, S, K, r, G, self.layout)
+
+    def info(self):
+        return wa_plan_info(self.handle)
+
+    def forward(self, q, k, v, out=None, stream=None):
+        """out <- window attention of bf16 CUDA tensors q, k, v (shape [B, L, H, D], this plan's layout)."""
+        import torch
+        lay = self.layout
+        shape = (lay.B, self.L, lay.H, lay.D)
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or tuple(t.shape) != shape:
+                raise ValueError(f"{name} must be a bf16 CUDA tensor of shape {shape}")
+            if tuple(t.stride()) != (lay.stride_b, lay.stride_l, lay.stride_h, 1):
+                raise ValueError(f"{name} strides {t.stride()} differ from the plan's layout")
+        if out is None:
+            out = torch.empty_strided(shape, (lay.stride_b, lay.stride_l, lay.stride_h, 1), dtype=torch.bfloat16,
+                                      device=q.device)
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        wa_forward(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), s.cuda_stream)
+        return out
+
+    def check_error(self, stream=None):
+        import torch
+        s = torch.cuda.current_stream() if stream is None else stream
+        return wa_plan_check_error(self.handle, s.cuda_stream)
+
+    def set_debug_flags(self, flags):
+        _check(lib().wa_plan_set_debug_flags(self.handle, flags), "wa_plan_set_debug_flags")
+
+    def close(self):
+        if getattr(self, "handle", None) is not None:
+            wa_plan_release(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def forward(q, k, v, T, S, K, r, G, global_pos=0, out=None):
+    """One-shot call: out = window attention of q, k, v ([B, L, H, D] bf16 on a CUDA device).
+
+    CPU tensors are accepted too (end-to-end use): they are copied to the current CUDA device (from pinned memory
+    when they are pinned), the attention runs there, and the result is copied back into a CPU tensor.
+    """
+    import torch
+    B, L, H, D = q.shape
+    on_host = not q.is_cuda
+    if on_host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
+    else:
+        qd, kd, vd = q, k, v
+    plan = Plan(T, S, K, r, G, B, H, D, global_pos)
+    try:
+        od = plan.forward(qd, kd, vd, out=None if on_host else out)
+    finally:
+        plan.close()
+    if on_host:
+        res = out if out is not None else torch.empty(od.shape, dtype=od.dtype, pin_memory=q.is_pinned())
+        res.copy_(od, non_blocking=False)
+        return res
+    return od

@@ -1,0 +1,71 @@
+// Internal declarations shared by the host plan/ABI code and the CUDA launchers.
+#pragma once
+
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/wa.h"
+
+namespace wa {
+
+constexpr int kTileRows = 128;    // query rows per tile and key rows per key tile
+constexpr int kItemQTiles = 2;    // query tiles per work item (they share the key tiles)
+constexpr int kItemRows = kTileRows * kItemQTiles;
+
+// One work item of the attention kernel, 8 x int32 (two 16-byte loads on the device).
+//   split < 0: window item, the query rows [q_lo, q_hi) are written as bf16 rows of `out`.
+//   split >= 0: global-leg item, the rows are written as fp32 partials + log2-sum-exp to the workspace at
+//               split index `split`.
+// Keys: segment 0 [s0_lo, s0_hi) then segment 1 [s1_lo, s1_hi) (empty when equal), processed in key tiles of
+// kTileRows rows; the last tile of each segment is column-masked.
+struct Item {
+  int32_t bh, split, q_lo, q_hi, s0_lo, s0_hi, s1_lo, s1_hi;
+};
+static_assert(sizeof(Item) == 32, "work item is 32 bytes");
+
+struct Geometry {
+  int T, S, K, r, G;
+  wa_layout_t layout;
+  int64_t nc, F, L, f0, g0;
+};
+
+struct HostPlan {
+  Geometry geo;
+  wa_plan_info_t info;
+  std::vector<wa_group_t> groups;
+  std::vector<Item> items;
+  int n_splits;
+};
+
+// Validate arguments; on success fill `geo`.
+wa_status make_geometry(int T, int S, int K, int r, int G, const wa_layout_t* layout, Geometry* geo);
+// Build groups, splits and the ordered work list on the host.
+void build_host_plan(const Geometry& geo, HostPlan* hp);
+
+// Arguments of one attention launch (device pointers; tensor maps are built by the launcher).
+struct LaunchArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const Item* items;
+  int n_items;
+  float* ws_o;      // [B*H][G][n_splits][D] fp32 (global leg partial outputs, normalised per split)
+  float* ws_lse;    // [B*H][G][n_splits] fp32 (log2-domain log-sum-exp of the scaled scores per split)
+  int* err;         // device error word
+  int n_splits;
+  int debug_flags;  // test-only fault injection on the host-visible error path (0 in normal use)
+  const Geometry* geo;
+};
+
+// Encode the tensor maps and launch the attention kernel; returns a CUDA error code (0 on success).
+int launch_attention(const LaunchArgs& a, void* stream, int num_sms);
+// Launch the log-sum-exp merge of the global rows; returns a CUDA error code.
+int launch_combine(const LaunchArgs& a, void* stream);
+
+// Device error word bits.
+constexpr int kErrTimeout = 1;
+constexpr int kErrBounds = 2;
+
+}  // namespace wa

@@ -1,0 +1,559 @@
+// Attention kernels for chunk-aligned window softmax attention on sm_103a.
+//
+// One persistent launch runs every work item of the plan: window items (a pair of 128-row query tiles of one
+// window group against the group's key segments: its frame window, then the globals) and global-leg items (a
+// pair of global query tiles against one key split of the whole sequence). This is the decomposition of the
+// VDN-Minimax-H3 window-attention article, section 三: every kept (query, key) pair lies in a dense rectangle,
+// and each rectangle is computed as plain dense attention with no mask except at segment tails.
+//
+// CTA roles (320 threads, one CTA per SM):
+//   warps 0-3  softmax warpgroup of query tile 0: one thread per query row / TMEM lane
+//   warps 4-7  softmax warpgroup of query tile 1
+//   warp 8     MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V with tcgen05.mma, accumulators in TMEM
+//   warp 9     TMA producer (one thread): Q tiles and a ring of K / V tiles, 128-byte swizzled
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [384, 384+D). P_t (bf16) overwrites the
+// first 64 columns of S_t and is the A operand of the P.V MMA, read straight from TMEM.
+// The two query tiles ping-pong: while one warpgroup runs the softmax of its tile, the tensor core works on the
+// other tile's products.
+//
+// Softmax state is fp32 in registers: running max m (in log2 units of the scaled score) and row sum l. The max
+// is only raised when it grows by more than 2^8, so the O rescale in TMEM is rare; this is exact because the
+// final normalisation uses the same m. Every wait is bounded; on expiry the kernel latches an error in the plan's
+// error word and unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "wa_internal.h"
+#include "wa_ptx.cuh"
+
+namespace wa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O only when the max grows by > 2^8
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms: waiting for in-flight copies while unwinding
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;              // 128-byte swizzle boxes per row
+  static constexpr int kHalfBytes = kTileRows * 128;  // one box: 128 rows x 64 bf16
+  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kSlots = D == 128 ? 4 : 8;  // K / V ring
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
+  // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain kv_full[kSlots] kv_empty[kSlots]
+  static constexpr int kNumBars = 11 + 2 * kSlots;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t kTmemO = 256;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);   // P from TMEM, V MN-major (D contiguous)
+};
+
+struct Params {
+  const Item* items;
+  int n_items;
+  __nv_bfloat16* out;
+  float* ws_o;
+  float* ws_lse;
+  int* err;
+  int64_t sb, sl, sh;  // element strides of out
+  int H, G, g0, n_splits;
+  float c_scale;  // log2(e) / sqrt(D)
+  int debug_flags;
+};
+
+// Shared-memory barrier layout, relative to the barrier block: q_full[2] q_empty[2] s_full[2] p_full[2]
+// o_full[2] drain kv_full[kSlots] kv_empty[kSlots]. Addresses are computed, never indexed from a local array.
+struct BarAddr {
+  uint32_t base;
+  __device__ __forceinline__ uint32_t q_full(int t) const { return base + 8 * (0 + t); }
+  __device__ __forceinline__ uint32_t q_empty(int t) const { return base + 8 * (2 + t); }
+  __device__ __forceinline__ uint32_t s_full(int t) const { return base + 8 * (4 + t); }
+  __device__ __forceinline__ uint32_t p_full(int t) const { return base + 8 * (6 + t); }
+  __device__ __forceinline__ uint32_t o_full(int t) const { return base + 8 * (8 + t); }
+  __device__ __forceinline__ uint32_t drain() const { return base + 8 * 10; }
+  __device__ __forceinline__ uint32_t kv_full(uint32_t slot) const { return base + 8 * (11 + slot); }
+  template <int kSlots>
+  __device__ __forceinline__ uint32_t kv_empty(uint32_t slot) const { return base + 8 * (11 + kSlots + slot); }
+};
+
+__device__ __forceinline__ Item load_item(const Item* items, int idx) {
+  const int4* p = reinterpret_cast<const int4*>(items + idx);
+  int4 a = __ldg(p), b = __ldg(p + 1);
+  return Item{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+}
+
+__device__ __forceinline__ int seg_tiles(int lo, int hi) { return hi > lo ? (hi - lo + kTileRows - 1) / kTileRows : 0; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    window_attention_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v, const Params prm) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ = s_base + C::kQOff;
+  const uint32_t sKV = s_base + C::kKVOff;
+  const uint32_t bar0 = s_base + C::kBarOff;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+  const BarAddr bars{bar0};
+  auto kv_empty = [&](uint32_t slot) { return bars.kv_empty<C::kSlots>(slot); };
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid == 0) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.q_full(t), 1);
+      mbar_init(bars.q_empty(t), 1);
+      mbar_init(bars.s_full(t), 1);
+      mbar_init(bars.p_full(t), 128);
+      mbar_init(bars.o_full(t), 1);
+    }
+    mbar_init(bars.drain(), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bars.kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  int* err = prm.err;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kv_n = 0;
+      uint32_t q_n0 = 0, q_n1 = 0;
+      bool dropped = false;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+        const Item it = load_item(prm.items, idx);
+        const int b = it.bh / prm.H, h = it.bh % prm.H;
+        const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= ntq || !ok) break;
+          uint32_t& qn = t ? q_n1 : q_n0;
+          ok = mbar_wait(bars.q_empty(t), (qn & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bars.q_full(t), C::kTileBytes);
+#pragma unroll
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_4d(sQ + t * C::kTileBytes + hf * C::kHalfBytes, &tmap_q, bars.q_full(t), hf * 64, h,
+                        it.q_lo + t * kTileRows, b);
+          qn++;
+        }
+        const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
+        const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+        for (int j = 0; j < nt && ok; ++j) {
+          const int row = j < nt0 ? it.s0_lo + j * kTileRows : it.s1_lo + (j - nt0) * kTileRows;
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t slot = kv_n % C::kSlots;
+            ok = mbar_wait(kv_empty(slot), ((kv_n / C::kSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            if (!ok) break;
+            if ((prm.debug_flags & 1) && !dropped && blockIdx.x == 0) {
+              dropped = true;  // fault injection for the watchdog test: this tile is never loaded
+            } else {
+              mbar_arrive_expect_tx(bars.kv_full(slot), C::kTileBytes);
+#pragma unroll
+              for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_load_4d(sKV + slot * C::kTileBytes + hf * C::kHalfBytes, which ? &tmap_v : &tmap_k,
+                            bars.kv_full(slot), hf * 64, h, row, b);
+            }
+            kv_n++;
+          }
+        }
+      }
+      if (!ok) {
+        // Unwinding: wait (briefly) for the copies still in flight so that none lands after the CTA exits.
+        for (uint32_t n = kv_n > (uint32_t)C::kSlots ? kv_n - C::kSlots : 0; n < kv_n; ++n)
+          mbar_wait_drain(bars.kv_full(n % C::kSlots), (n / C::kSlots) & 1, kDrainLimitNs);
+        if (q_n0) mbar_wait_drain(bars.q_full(0), (q_n0 - 1) & 1, kDrainLimitNs);
+        if (q_n1) mbar_wait_drain(bars.q_full(1), (q_n1 - 1) & 1, kDrainLimitNs);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t kv_n = 0;
+      uint32_t q_n0 = 0, q_n1 = 0, p_n0 = 0, p_n1 = 0;
+      bool ok = true;
+      // O_t (+)= P_t V, P_t read from TMEM (aliasing S_t), V from the ring slot at `vaddr` (MN-major: D contiguous)
+      auto issue_pv = [&](int t, uint32_t vaddr, bool acc_first) {
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_ts(tmem + C::kTmemO + t * 128, tmem + t * 128 + kk * 8,
+                 sdesc_sw128(vaddr + kk * 2048, C::kHalfBytes, 1024), C::kIdescPV, (acc_first || kk > 0) ? 1u : 0u);
+      };
+      // S_t = Q_t K^T, both K-major; K = D advances 32 bytes inside a 128-byte swizzle row, then to the next box
+      auto issue_s = [&](int t, uint32_t kaddr) {
+        const uint32_t qaddr = sQ + t * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+          mma_ss(tmem + t * 128, sdesc_sw128(qaddr + off, 16, 1024), sdesc_sw128(kaddr + off, 16, 1024), C::kIdescS,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+        const Item it = load_item(prm.items, idx);
+        const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+        const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
+        const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+        ok = mbar_wait(bars.q_full(0), q_n0 & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        q_n0++;
+        if (ok && ntq > 1) {
+          ok = mbar_wait(bars.q_full(1), q_n1 & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          q_n1++;
+        }
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t prev_vslot = 0, prev_vpar = 0;
+        for (int j = 0; j < nt; ++j) {
+          const uint32_t kslot = kv_n % C::kSlots, kpar = (kv_n / C::kSlots) & 1;
+          ++kv_n;
+          const uint32_t vslot = kv_n % C::kSlots, vpar = (kv_n / C::kSlots) & 1;
+          ++kv_n;
+          ok = mbar_wait(bars.kv_full(kslot), kpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          if (ok && j > 0) ok = mbar_wait(bars.kv_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kaddr = sKV + kslot * C::kTileBytes;
+          const uint32_t vaddr_prev = sKV + prev_vslot * C::kTileBytes;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= ntq) break;
+            if (j > 0) {
+              uint32_t& pn = t ? p_n1 : p_n0;
+              ok = mbar_wait(bars.p_full(t), pn & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              pn++;
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, vaddr_prev, j > 1);  // O_t += P_t(j-1) V_{j-1}
+            }
+            issue_s(t, kaddr);  // S_t = Q_t K_j^T
+            mma_commit(bars.s_full(t));
+          }
+          if (!ok) break;
+          mma_commit(kv_empty(kslot));
+          if (j > 0) mma_commit(kv_empty(prev_vslot));
+          if (j == nt - 1) {
+            mma_commit(bars.q_empty(0));
+            if (ntq > 1) mma_commit(bars.q_empty(1));
+          }
+          prev_vslot = vslot;
+          prev_vpar = vpar;
+        }
+        if (!ok) break;
+        ok = mbar_wait(bars.kv_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vaddr = sKV + prev_vslot * C::kTileBytes;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= ntq) break;
+          uint32_t& pn = t ? p_n1 : p_n0;
+          ok = mbar_wait(bars.p_full(t), pn & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          pn++;
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, vaddr, nt > 1);
+          mma_commit(bars.o_full(t));
+        }
+        if (!ok) break;
+        mma_commit(kv_empty(prev_vslot));
+      }
+      // Every MMA and every completion arrive must have landed before the CTA tears down.
+      mma_commit(bars.drain());
+      mbar_wait_drain(bars.drain(), 0, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    // ---------------------------------------------------------------------------------- softmax warpgroups
+    const int t = warp >> 2;            // query tile of this warpgroup
+    const int row_in_tile = tid & 127;  // == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + C::kTmemO + t * 128;
+    const uint32_t bar_s = bars.s_full(t), bar_p = bars.p_full(t), bar_o = bars.o_full(t);
+    uint32_t s_n = 0, o_n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+      const Item it = load_item(prm.items, idx);
+      const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+      if (t >= ntq) continue;
+      const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
+      const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        const int valid = j < nt0 ? min(kTileRows, it.s0_hi - (it.s0_lo + j * kTileRows))
+                                  : min(kTileRows, it.s1_hi - (it.s1_lo + (j - nt0) * kTileRows));
+        ok = mbar_wait(bar_s, s_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        s_n++;
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld_x128(tS, sr);
+        float* s = reinterpret_cast<float*>(sr);
+        if (valid < kTileRows) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= valid) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * prm.c_scale;
+        if (j == 0) {
+          m = m_cand;
+        } else {
+          const bool need = m_cand > m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2(m - m_cand) : 1.f;
+            if (need) m = m_cand;
+            l *= alpha;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld_x32(tO + c0, o);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              tmem_st_x32(tO + c0, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        const float neg_m = -m;
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // P(bf16) for 64 key columns -> 32 TMEM columns over S
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2(fmaf(s[64 * half + 2 * c], prm.c_scale, neg_m));
+            const float p1 = ex2(fmaf(s[64 * half + 2 * c + 1], prm.c_scale, neg_m));
+            sum0 += p0;
+            sum1 += p1;
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+            pk[c] = *reinterpret_cast<uint32_t*>(&v2);
+          }
+          tmem_st_x32(tS + 32 * half, pk);
+        }
+        l += sum0 + sum1;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_p);
+      }
+      if (!ok) break;
+      ok = mbar_wait(bar_o, o_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      o_n++;
+      if (!ok) break;
+      tc_fence_after();
+      // Epilogue: O / l, straight into this row's place (no scatter pass).
+      const int row = it.q_lo + t * kTileRows + row_in_tile;
+      const bool row_ok = row < it.q_hi;
+      const float inv_l = 1.f / l;
+      const int b = it.bh / prm.H, h = it.bh % prm.H;
+      if (it.split < 0) {
+        __nv_bfloat16* dst = prm.out + (int64_t)b * prm.sb + (int64_t)row * prm.sl + (int64_t)h * prm.sh;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+          uint32_t w[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(o[2 * c]) * inv_l,
+                                                      __uint_as_float(o[2 * c + 1]) * inv_l);
+            w[c] = *reinterpret_cast<uint32_t*>(&v2);
+          }
+          if (row_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          }
+        }
+      } else {
+        const int64_t grow = (int64_t)row - prm.g0;
+        const int64_t slot = ((int64_t)it.bh * prm.G + grow) * prm.n_splits + it.split;
+        float* dst = prm.ws_o + slot * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+          if (row_ok) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c0);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              d4[c] = make_float4(__uint_as_float(o[4 * c]) * inv_l, __uint_as_float(o[4 * c + 1]) * inv_l,
+                                  __uint_as_float(o[4 * c + 2]) * inv_l, __uint_as_float(o[4 * c + 3]) * inv_l);
+          }
+        }
+        if (row_ok) prm.ws_lse[slot] = m + __log2f(l);
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    __syncwarp();  // tcgen05.dealloc is warp-collective: reconverge after the role branches
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge the key splits of the global rows: out = sum_p 2^(lse_p - lse*) O_p with lse* the log2-sum-exp of the
+// split values (each O_p is already normalised by its own row sum). One warp per global row.
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                                                      __nv_bfloat16* __restrict__ out, int rows, int G, int H, int g0,
+                                                      int P, int64_t sb, int64_t sl, int64_t sh) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  constexpr int kPer = D / 32;
+  const float* lse = ws_lse + (int64_t)r * P;
+  const float* o = ws_o + (int64_t)r * P * D;
+  float mx = -INFINITY;
+  for (int p = 0; p < P; ++p) mx = fmaxf(mx, __ldg(lse + p));
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float den = 0.f;
+  for (int p = 0; p < P; ++p) {
+    const float w = ex2(__ldg(lse + p) - mx);
+    den += w;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = fmaf(w, __ldg(o + (int64_t)p * D + lane + 32 * i), acc[i]);
+  }
+  const float inv = 1.f / den;
+  const int bh = r / G, gr = r % G;
+  const int b = bh / H, h = bh % H;
+  __nv_bfloat16* dst = out + (int64_t)b * sb + (int64_t)(g0 + gr) * sl + (int64_t)h * sh;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) dst[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 4-D map over (D, H, L, B) with a 64 x 1 x 128 x 1 box and 128-byte swizzle; rows past L read as zeros.
+bool make_map(CUtensorMap* m, const void* ptr, const Geometry& g) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const wa_layout_t& l = g.layout;
+  cuuint64_t dims[4] = {(cuuint64_t)l.D, (cuuint64_t)l.H, (cuuint64_t)g.L, (cuuint64_t)l.B};
+  cuuint64_t strides[3] = {(cuuint64_t)l.stride_h * 2, (cuuint64_t)l.stride_l * 2, (cuuint64_t)l.stride_b * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileRows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
+  using C = Cfg<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, *a.geo) || !make_map(&mk, a.k, *a.geo) || !make_map(&mv, a.v, *a.geo))
+    return (int)cudaErrorInvalidValue;
+  const wa_layout_t& l = a.geo->layout;
+  Params p;
+  p.items = a.items;
+  p.n_items = a.n_items;
+  p.out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  p.ws_o = a.ws_o;
+  p.ws_lse = a.ws_lse;
+  p.err = a.err;
+  p.sb = l.stride_b;
+  p.sl = l.stride_l;
+  p.sh = l.stride_h;
+  p.H = l.H;
+  p.G = a.geo->G;
+  p.g0 = (int)a.geo->g0;
+  p.n_splits = a.n_splits;
+  p.c_scale = (float)(1.4426950408889634 / sqrt((double)D));
+  p.debug_flags = a.debug_flags;
+  const int grid = a.n_items < num_sms ? a.n_items : num_sms;
+  window_attention_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_attention(const LaunchArgs& a, void* stream, int num_sms) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return a.geo->layout.D == 128 ? launch_attention_d<128>(a, s, num_sms) : launch_attention_d<64>(a, s, num_sms);
+}
+
+int launch_combine(const LaunchArgs& a, void* stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Geometry& g = *a.geo;
+  const wa_layout_t& l = g.layout;
+  const int rows = l.B * l.H * g.G;
+  const int blocks = (rows + 7) / 8;
+  if (l.D == 128)
+    combine_kernel<128><<<blocks, 256, 0, s>>>(a.ws_o, a.ws_lse, reinterpret_cast<__nv_bfloat16*>(a.out), rows, g.G,
+                                               l.H, (int)g.g0, a.n_splits, l.stride_b, l.stride_l, l.stride_h);
+  else
+    combine_kernel<64><<<blocks, 256, 0, s>>>(a.ws_o, a.ws_lse, reinterpret_cast<__nv_bfloat16*>(a.out), rows, g.G,
+                                              l.H, (int)g.g0, a.n_splits, l.stride_b, l.stride_l, l.stride_h);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace wa

@@ -1,0 +1,401 @@
+// Host side of the library: argument checks, the window-group plan, the work list, the plan cache and the C ABI.
+//
+// The plan follows the VDN-Minimax-H3 window-attention article, section 三 ("the mask is a union of a few dense
+// rectangles"): query rows whose kept key sets are identical form a group, and each group is one plain dense
+// attention. A chunk's kept set is its clamped frame window plus the globals (section 一), so groups are runs of
+// consecutive chunks whose clamped windows coincide. The article caches one plan per geometry, at most four
+// (section 三, _Plan); this cache does the same and evicts the least recently used unreferenced plan.
+#include <cuda_runtime_api.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <list>
+#include <mutex>
+
+#include "wa_internal.h"
+
+struct wa_plan {
+  wa::HostPlan hp;
+  int device = -1;
+  int num_sms = 0;
+  int refcount = 0;
+  bool cached = false;
+  uint64_t lru = 0;
+  wa::Item* d_items = nullptr;
+  float* d_ws = nullptr;  // partial outputs followed by the log-sum-exp values
+  int* d_err = nullptr;
+  int64_t ws_o_elems = 0;
+  cudaStream_t last_stream = nullptr;
+  bool have_last = false;
+  cudaEvent_t done = nullptr;
+  int debug_flags = 0;
+};
+
+namespace wa {
+
+static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+wa_status make_geometry(int T, int S, int K, int r, int G, const wa_layout_t* layout, Geometry* geo) {
+  if (!layout || !geo) return WA_ERR_INVALID;
+  if (T < 1 || S < 1 || K < 1 || r < 0 || G < 0) return WA_ERR_INVALID;
+  const wa_layout_t& l = *layout;
+  if (l.global_pos != 0 && l.global_pos != 1) return WA_ERR_INVALID;
+  if (l.B < 1 || l.H < 1 || l.D < 1) return WA_ERR_INVALID;
+  if (l.D != 64 && l.D != 128) return WA_ERR_UNSUPPORTED;
+  int64_t L = (int64_t)T * S + G;
+  if (L >= ((int64_t)1 << 31) - kTileRows) return WA_ERR_UNSUPPORTED;
+  if (l.stride_b < 1 || l.stride_l < 1 || l.stride_h < 1) return WA_ERR_INVALID;
+  if (l.stride_b % 8 || l.stride_l % 8 || l.stride_h % 8) return WA_ERR_INVALID;
+  // The strides must map distinct (b, l, h, d) to distinct elements: sort the outer axes by stride and check
+  // that each axis starts past the end of the previous ones (d is contiguous, extent D).
+  struct Ax { int64_t stride, extent; } ax[3] = {{l.stride_b, l.B}, {l.stride_l, L}, {l.stride_h, l.H}};
+  std::sort(ax, ax + 3, [](const Ax& a, const Ax& b) { return a.stride < b.stride; });
+  int64_t span = l.D;
+  for (auto& a : ax) {
+    if (a.extent == 1) continue;
+    if (a.stride < span) return WA_ERR_INVALID;
+    span = a.stride * a.extent;
+  }
+  geo->T = T; geo->S = S; geo->K = K; geo->r = r; geo->G = G;
+  geo->layout = l;
+  geo->nc = cdiv(T, K);
+  geo->F = (int64_t)T * S;
+  geo->L = L;
+  geo->f0 = l.global_pos ? G : 0;
+  geo->g0 = l.global_pos ? 0 : geo->F;
+  return WA_OK;
+}
+
+static int64_t seg_tiles(int64_t lo, int64_t hi) { return hi > lo ? cdiv(hi - lo, kTileRows) : 0; }
+
+void build_host_plan(const Geometry& g, HostPlan* hp) {
+  const int64_t KS = (int64_t)g.K * g.S;
+  hp->geo = g;
+  hp->groups.clear();
+  hp->items.clear();
+  // Window groups: runs of chunks with the same clamped window [max(0, c-r), min(nc-1, c+r)].
+  int64_t prev_lo = -1, prev_hi = -1;
+  for (int64_t c = 0; c < g.nc; ++c) {
+    int64_t lo = std::max<int64_t>(0, c - g.r), hi = std::min<int64_t>(g.nc - 1, c + g.r);
+    int64_t q_lo = g.f0 + c * KS, q_hi = g.f0 + std::min<int64_t>(g.T, (c + 1) * (int64_t)g.K) * g.S;
+    if (lo == prev_lo && hi == prev_hi) {
+      hp->groups.back().q_hi = q_hi;
+      continue;
+    }
+    prev_lo = lo; prev_hi = hi;
+    wa_group_t gr;
+    gr.q_lo = q_lo; gr.q_hi = q_hi;
+    gr.kv0_lo = g.f0 + lo * KS;
+    gr.kv0_hi = g.f0 + std::min<int64_t>(g.T, (hi + 1) * (int64_t)g.K) * g.S;
+    gr.kv1_lo = gr.kv1_hi = 0;
+    if (g.G > 0) {
+      if (gr.kv0_hi == g.g0) {              // globals right after the window: one contiguous segment
+        gr.kv0_hi = g.g0 + g.G;
+      } else if (g.g0 + g.G == gr.kv0_lo) {  // globals right before the window
+        gr.kv0_lo = g.g0;
+      } else {
+        gr.kv1_lo = g.g0; gr.kv1_hi = g.g0 + g.G;
+      }
+    }
+    hp->groups.push_back(gr);
+  }
+  // Split count of the global leg: splits about as long as the longest window item, so that every item of the
+  // persistent kernel costs about the same.
+  int64_t wmax = 1;
+  for (auto& gr : hp->groups) wmax = std::max(wmax, seg_tiles(gr.kv0_lo, gr.kv0_hi) + seg_tiles(gr.kv1_lo, gr.kv1_hi));
+  int64_t Lt = cdiv(g.L, kTileRows);
+  int n_splits = 1;
+  int64_t tps = Lt;
+  if (g.G > 0) {
+    int64_t p = std::min<int64_t>(64, std::max<int64_t>(1, cdiv(Lt, wmax)));
+    tps = cdiv(Lt, p);
+    n_splits = (int)cdiv(Lt, tps);
+  }
+  hp->n_splits = n_splits;
+
+  const int BH = g.layout.B * g.layout.H;
+  std::vector<Item> items;
+  for (int bh = 0; bh < BH; ++bh) {
+    for (auto& gr : hp->groups) {
+      for (int64_t q = gr.q_lo; q < gr.q_hi; q += kItemRows) {
+        Item it{bh, -1, (int32_t)q, (int32_t)std::min<int64_t>(gr.q_hi, q + kItemRows), (int32_t)gr.kv0_lo,
+                (int32_t)gr.kv0_hi, (int32_t)gr.kv1_lo, (int32_t)gr.kv1_hi};
+        items.push_back(it);
+      }
+    }
+    if (g.G > 0) {
+      for (int64_t q = g.g0; q < g.g0 + g.G; q += kItemRows) {
+        for (int p = 0; p < n_splits; ++p) {
+          int64_t lo = (int64_t)p * tps * kTileRows, hi = std::min<int64_t>(g.L, (int64_t)(p + 1) * tps * kTileRows);
+          Item it{bh, p, (int32_t)q, (int32_t)std::min<int64_t>(g.g0 + g.G, q + kItemRows), (int32_t)lo,
+                  (int32_t)hi, 0, 0};
+          items.push_back(it);
+        }
+      }
+    }
+  }
+  // Longest first (stable, so the items of one group and head stay adjacent and share keys in L2).
+  auto tiles = [](const Item& it) { return seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi); };
+  std::stable_sort(items.begin(), items.end(), [&](const Item& a, const Item& b) { return tiles(a) > tiles(b); });
+  hp->items = std::move(items);
+
+  wa_plan_info_t& in = hp->info;
+  memset(&in, 0, sizeof(in));
+  in.n_chunks = (int32_t)g.nc;
+  in.n_groups = (int32_t)hp->groups.size();
+  in.n_splits = n_splits;
+  in.n_items = (int32_t)hp->items.size();
+  in.L = g.L;
+  int64_t wp = 0;
+  for (auto& gr : hp->groups) wp += (gr.q_hi - gr.q_lo) * ((gr.kv0_hi - gr.kv0_lo) + (gr.kv1_hi - gr.kv1_lo));
+  in.window_pairs = wp;
+  in.global_pairs = (int64_t)g.G * g.L;
+  in.kept_pairs = wp + in.global_pairs;
+  in.workspace_bytes = g.G > 0 ? (int64_t)BH * g.G * n_splits * (g.layout.D + 1) * 4 : 0;
+  int64_t kt = 0;
+  for (auto& it : hp->items) kt += tiles(it);
+  in.kv_tiles = kt;
+}
+
+}  // namespace wa
+
+// ------------------------------------------------------------------------------------------- plan cache
+namespace {
+
+std::mutex g_mu;
+std::list<wa_plan*> g_cache;  // cached plans (referenced or not)
+uint64_t g_tick = 0;
+constexpr size_t kMaxCached = 4;
+
+bool same_key(const wa_plan* p, int dev, const wa::Geometry& g) {
+  const wa::Geometry& a = p->hp.geo;
+  return p->device == dev && a.T == g.T && a.S == g.S && a.K == g.K && a.r == g.r && a.G == g.G &&
+         memcmp(&a.layout, &g.layout, sizeof(wa_layout_t)) == 0;
+}
+
+void free_plan(wa_plan* p) {
+  if (!p) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (p->device >= 0 && cur != p->device) cudaSetDevice(p->device);
+  if (p->d_items) cudaFree(p->d_items);
+  if (p->d_ws) cudaFree(p->d_ws);
+  if (p->d_err) cudaFree(p->d_err);
+  if (p->done) cudaEventDestroy(p->done);
+  if (p->device >= 0 && cur >= 0 && cur != p->device) cudaSetDevice(cur);
+  delete p;
+}
+
+bool env_flag(const char* name) {
+  const char* s = getenv(name);
+  return s && s[0] && strcmp(s, "0") != 0;
+}
+
+template <class T>
+cudaError_t dev_alloc(T** ptr, size_t bytes) {
+  if (env_flag("WA_TEST_FAIL_ALLOC")) {
+    *ptr = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc((void**)ptr, bytes);
+}
+
+wa_status create_uncached(const wa::Geometry& g, int dev, wa_plan** out) {
+  wa_plan* p = new wa_plan();
+  p->device = dev;
+  wa::build_host_plan(g, &p->hp);
+  if (cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    delete p;
+    return WA_ERR_CUDA;
+  }
+  const size_t items_bytes = std::max<size_t>(1, p->hp.items.size()) * sizeof(wa::Item);
+  const wa_plan_info_t& in = p->hp.info;
+  p->ws_o_elems = (int64_t)g.layout.B * g.layout.H * g.G * p->hp.n_splits * g.layout.D;
+  cudaError_t e = dev_alloc(&p->d_items, items_bytes);
+  if (e == cudaSuccess && in.workspace_bytes > 0) e = dev_alloc(&p->d_ws, (size_t)in.workspace_bytes);
+  if (e == cudaSuccess) e = dev_alloc(&p->d_err, sizeof(int));
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free allocation error
+    free_plan(p);
+    return e == cudaErrorMemoryAllocation ? WA_ERR_OOM : WA_ERR_CUDA;
+  }
+  if (cudaMemcpy(p->d_items, p->hp.items.data(), p->hp.items.size() * sizeof(wa::Item), cudaMemcpyHostToDevice) !=
+          cudaSuccess ||
+      cudaMemset(p->d_err, 0, sizeof(int)) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) != cudaSuccess) {
+    free_plan(p);
+    return WA_ERR_CUDA;
+  }
+  if (env_flag("WA_LOG")) {
+    fprintf(stderr,
+            "[wa] plan T=%d S=%d K=%d r=%d G=%d B=%d H=%d D=%d: %d groups, %d splits, %d items, %lld kept pairs/head, "
+            "workspace %lld B\n",
+            g.T, g.S, g.K, g.r, g.G, g.layout.B, g.layout.H, g.layout.D, in.n_groups, in.n_splits, in.n_items,
+            (long long)in.kept_pairs, (long long)in.workspace_bytes);
+  }
+  *out = p;
+  return WA_OK;
+}
+
+bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) { return a < b + nb && b < a + na; }
+
+}  // namespace
+
+extern "C" {
+
+const char* wa_status_string(wa_status s) {
+  switch (s) {
+    case WA_OK: return "WA_OK";
+    case WA_ERR_INVALID: return "WA_ERR_INVALID";
+    case WA_ERR_UNSUPPORTED: return "WA_ERR_UNSUPPORTED";
+    case WA_ERR_OOM: return "WA_ERR_OOM";
+    case WA_ERR_CUDA: return "WA_ERR_CUDA";
+    case WA_ERR_DEVICE_TIMEOUT: return "WA_ERR_DEVICE_TIMEOUT";
+    case WA_ERR_DEVICE_BOUNDS: return "WA_ERR_DEVICE_BOUNDS";
+  }
+  return "WA_UNKNOWN";
+}
+
+wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, wa_plan_info_t* info,
+                               wa_group_t* groups, int64_t groups_cap, int64_t* items, int64_t items_cap) {
+  if (!info) return WA_ERR_INVALID;
+  wa::Geometry g;
+  wa_status st = wa::make_geometry(T, S, K, r, G, layout, &g);
+  if (st != WA_OK) return st;
+  wa::HostPlan hp;
+  wa::build_host_plan(g, &hp);
+  *info = hp.info;
+  if (groups)
+    for (int64_t i = 0; i < std::min<int64_t>(groups_cap, (int64_t)hp.groups.size()); ++i) groups[i] = hp.groups[i];
+  if (items)
+    for (int64_t i = 0; i < std::min<int64_t>(items_cap, (int64_t)hp.items.size()); ++i) {
+      const wa::Item& it = hp.items[i];
+      int64_t* o = items + 8 * i;
+      o[0] = it.bh; o[1] = it.split < 0 ? 0 : 1; o[2] = it.q_lo; o[3] = it.q_hi;
+      o[4] = it.s0_lo; o[5] = it.s0_hi; o[6] = it.s1_lo; o[7] = it.s1_hi;
+    }
+  return WA_OK;
+}
+
+wa_status wa_plan_create(int T, int S, int K, int r, int G, const wa_layout_t* layout, wa_plan_t** out) {
+  if (!out) return WA_ERR_INVALID;
+  *out = nullptr;
+  wa::Geometry g;
+  wa_status st = wa::make_geometry(T, S, K, r, G, layout, &g);
+  if (st != WA_OK) return st;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return WA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (wa_plan* p : g_cache) {
+    if (same_key(p, dev, g)) {
+      p->refcount++;
+      p->lru = ++g_tick;
+      *out = p;
+      return WA_OK;
+    }
+  }
+  wa_plan* p = nullptr;
+  st = create_uncached(g, dev, &p);
+  if (st != WA_OK) return st;
+  p->refcount = 1;
+  p->lru = ++g_tick;
+  // Make room: evict least recently used unreferenced plans; if every cached plan is in use, this one stays
+  // uncached and is freed on its last release.
+  while (g_cache.size() >= kMaxCached) {
+    wa_plan* victim = nullptr;
+    for (wa_plan* c : g_cache)
+      if (c->refcount == 0 && (!victim || c->lru < victim->lru)) victim = c;
+    if (!victim) break;
+    g_cache.remove(victim);
+    free_plan(victim);
+  }
+  if (g_cache.size() < kMaxCached) {
+    p->cached = true;
+    g_cache.push_back(p);
+  }
+  *out = p;
+  return WA_OK;
+}
+
+void wa_plan_release(wa_plan_t* plan) {
+  if (!plan) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (plan->refcount > 0) plan->refcount--;
+  if (plan->refcount == 0 && !plan->cached) free_plan(plan);
+}
+
+wa_status wa_plan_info(const wa_plan_t* plan, wa_plan_info_t* info) {
+  if (!plan || !info) return WA_ERR_INVALID;
+  *info = plan->hp.info;
+  return WA_OK;
+}
+
+// Test hook (not in the public header): set fault-injection flags of a plan.
+int wa_plan_set_debug_flags(wa_plan_t* plan, int flags) {
+  if (!plan) return WA_ERR_INVALID;
+  plan->debug_flags = flags;
+  return WA_OK;
+}
+
+// Test hook: number of cached plans and the reference count of a plan.
+int wa_cache_size(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return (int)g_cache.size();
+}
+int wa_plan_refcount(const wa_plan_t* plan) { return plan ? plan->refcount : -1; }
+
+wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream) {
+  if (!plan || !q || !k || !v || !out) return WA_ERR_INVALID;
+  auto al = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
+  if (!al(q) || !al(k) || !al(v) || !al(out)) return WA_ERR_INVALID;
+  const wa::Geometry& g = plan->hp.geo;
+  const wa_layout_t& l = g.layout;
+  const size_t span = 2 * (size_t)((l.B - 1) * l.stride_b + (g.L - 1) * l.stride_l + (l.H - 1) * l.stride_h + l.D);
+  uintptr_t o = (uintptr_t)out;
+  if (ranges_overlap(o, span, (uintptr_t)q, span) || ranges_overlap(o, span, (uintptr_t)k, span) ||
+      ranges_overlap(o, span, (uintptr_t)v, span))
+    return WA_ERR_INVALID;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) {
+    cudaGetLastError();
+    return WA_ERR_INVALID;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (plan->have_last && plan->last_stream != s) {
+    if (cudaStreamWaitEvent(s, plan->done, 0) != cudaSuccess) return WA_ERR_CUDA;
+  }
+  wa::LaunchArgs a;
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.items = plan->d_items;
+  a.n_items = (int)plan->hp.items.size();
+  a.ws_o = plan->d_ws;
+  a.ws_lse = plan->d_ws ? plan->d_ws + plan->ws_o_elems : nullptr;
+  a.err = plan->d_err;
+  a.n_splits = plan->hp.n_splits;
+  a.debug_flags = plan->debug_flags;
+  a.geo = &g;
+  if (a.n_items > 0 && wa::launch_attention(a, (void*)s, plan->num_sms) != 0) return WA_ERR_CUDA;
+  if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
+  if (cudaEventRecord(plan->done, s) != cudaSuccess) return WA_ERR_CUDA;
+  plan->last_stream = s;
+  plan->have_last = true;
+  return WA_OK;
+}
+
+wa_status wa_plan_check_error(wa_plan_t* plan, wa_stream_t stream) {
+  if (!plan) return WA_ERR_INVALID;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return WA_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, plan->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return WA_ERR_CUDA;
+  if (h && cudaMemset(plan->d_err, 0, sizeof(int)) != cudaSuccess) return WA_ERR_CUDA;
+  if (h & wa::kErrTimeout) return WA_ERR_DEVICE_TIMEOUT;
+  if (h & wa::kErrBounds) return WA_ERR_DEVICE_BOUNDS;
+  return WA_OK;
+}
+
+}  // extern "C"

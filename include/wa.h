@@ -1,0 +1,149 @@
+/*
+ * wa.h -- chunk-aligned window softmax attention for GB300 (sm_103a): the C ABI.
+ *
+ * The operation (VDN-Minimax-H3 window-attention article, lqnn.cn, sections 一 and 三):
+ *   The packed sequence holds T latent frames of S spatial tokens each plus G global (text/audio) tokens,
+ *   L = T*S + G rows. Frames are grouped into chunks of K consecutive frames (chunk c = floor(t / K); the
+ *   last chunk may be partial). A query token of a frame in chunk c attends to every token of the chunks in
+ *   [c - r, c + r] that exist, plus all G global tokens; a global query attends to all L tokens. Each query's
+ *   softmax is normalised over exactly that kept set; scores are scaled by 1/sqrt(D); non-causal.
+ *   The library computes it the article's "decomposed" way (section 三): query rows with identical kept sets
+ *   form a group and each group is one dense attention over its frame window plus the globals (the window
+ *   leg); the G global rows run one dense attention over the whole sequence (the global leg, split along the
+ *   keys and merged by log-sum-exp). The legs write disjoint row sets straight into the output.
+ *
+ * Layout: q, k, v and out are bf16 device tensors of logical shape [B, L, H, D] with the element strides given
+ * in wa_layout_t (the D axis contiguous). Frame token (t, s) is row f0 + t*S + s, global token g is row g0 + g,
+ * where (f0, g0) = (0, T*S) when global_pos == 0 (globals after the frames) and (G, 0) when global_pos == 1.
+ *
+ * Threading: every function may be called from any host thread; the plan cache is mutex-guarded.
+ * Errors: argument errors are returned synchronously and launch nothing. Device-side watchdog and bounds
+ * failures are latched in the plan and reported by wa_plan_check_error().
+ */
+#ifndef WA_H_
+#define WA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (a CUDA runtime/driver stream handle). NULL is the legacy default stream. */
+typedef struct CUstream_st* wa_stream_t;
+
+typedef enum {
+  WA_OK = 0,
+  WA_ERR_INVALID = 1,         /* bad argument: geometry, pointer, alignment, stride, aliasing */
+  WA_ERR_UNSUPPORTED = 2,     /* valid but not built: head dim other than 64/128, sizes past int32 rows */
+  WA_ERR_OOM = 3,             /* device allocation of the plan's tables or workspace failed */
+  WA_ERR_CUDA = 4,            /* a CUDA call failed (launch error, no device, wrong architecture) */
+  WA_ERR_DEVICE_TIMEOUT = 5,  /* a device-side wait ran past its limit; the kernel gave up and returned */
+  WA_ERR_DEVICE_BOUNDS = 6    /* a device-side index check failed; the access was skipped */
+} wa_status;
+
+/* How the four tensors are laid out. All four (q, k, v, out) share it. */
+typedef struct {
+  int32_t global_pos; /* 0 = globals after the frame tokens, 1 = before them */
+  int32_t B;          /* batch */
+  int32_t H;          /* heads */
+  int32_t D;          /* head dim: 64 or 128 */
+  int64_t stride_b;   /* element stride between batch entries; multiple of 8 */
+  int64_t stride_l;   /* element stride between sequence rows; multiple of 8 */
+  int64_t stride_h;   /* element stride between heads; multiple of 8 (contiguous: D) */
+} wa_layout_t;
+
+/* Counts describing a plan (host-side facts; filled by wa_plan_info and wa_geometry_describe). */
+typedef struct {
+  int32_t n_chunks;        /* ceil(T / K) */
+  int32_t n_groups;        /* window groups: chunks with identical clamped windows are merged */
+  int32_t n_splits;        /* key splits of the global leg (1 when G == 0) */
+  int32_t n_items;         /* work items of the attention kernel (window tiles + global split tiles) */
+  int64_t L;               /* T*S + G */
+  int64_t kept_pairs;      /* kept (query, key) pairs per (b, h) slice */
+  int64_t window_pairs;    /* of which: frame-query pairs */
+  int64_t global_pairs;    /* of which: global-query pairs (G * L) */
+  int64_t workspace_bytes; /* device workspace of the global leg: B*H*G*n_splits*(D+1)*4 */
+  int64_t kv_tiles;        /* sum over items of the key tiles each processes */
+} wa_plan_info_t;
+
+/* Per-group row of the window plan (wa_geometry_describe): all indices are sequence rows, half-open. */
+typedef struct {
+  int64_t q_lo, q_hi;   /* query rows of the group */
+  int64_t kv0_lo, kv0_hi; /* key segment 0: the window's frame tokens (merged with the globals when adjacent) */
+  int64_t kv1_lo, kv1_hi; /* key segment 1: the global tokens, or empty (lo == hi) */
+} wa_group_t;
+
+typedef struct wa_plan wa_plan_t;
+
+/*
+ * Build (or fetch from the cache) the plan for one geometry on the current CUDA device.
+ *   T, S, K >= 1; r >= 0 (r >= number of chunks is valid: dense attention); G >= 0 (0 runs no global leg).
+ *   layout: see wa_layout_t; B, H >= 1; D in {64, 128}; T*S + G < 2^31.
+ * The plan holds the window groups, the work list of the attention kernel (uploaded to the device once) and
+ * the global leg's workspace. Plans live in a process-wide cache of up to 4 geometries keyed on (device,
+ * geometry, layout); the least recently used unreferenced entry is evicted. Each successful call returns a
+ * reference that the caller must drop with wa_plan_release().
+ * Errors: WA_ERR_INVALID (null pointers, bad geometry), WA_ERR_UNSUPPORTED (D), WA_ERR_OOM, WA_ERR_CUDA.
+ */
+wa_status wa_plan_create(int T, int S, int K, int r, int G, const wa_layout_t* layout, wa_plan_t** out);
+
+/*
+ * out <- window attention of (q, k, v), asynchronously on `stream`.
+ *   q, k, v: device pointers to bf16 [B, L, H, D] (layout of the plan); read only.
+ *   out: device pointer to bf16 [B, L, H, D]; every element is overwritten; must not overlap q, k or v.
+ * Pointers must be 16-byte aligned. Host work is argument checks and building three TMA descriptors; the
+ * device work is two launches (the attention kernel over the plan's work list, then the log-sum-exp merge of
+ * the global rows). Forwards on one plan are serialised: a call on a different stream than the previous call
+ * first waits for that call to finish on the device, since both use the plan's workspace.
+ * Errors (synchronous, nothing launched): WA_ERR_INVALID for null/misaligned/overlapping pointers;
+ * WA_ERR_CUDA when a launch fails. Device-side failures: see wa_plan_check_error().
+ */
+wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device error word.
+ * Returns WA_OK, WA_ERR_DEVICE_TIMEOUT, WA_ERR_DEVICE_BOUNDS, or WA_ERR_CUDA if the synchronisation failed.
+ */
+wa_status wa_plan_check_error(wa_plan_t* plan, wa_stream_t stream);
+
+/* Counts of a plan. Errors: WA_ERR_INVALID for null pointers. */
+wa_status wa_plan_info(const wa_plan_t* plan, wa_plan_info_t* info);
+
+/* Drop one reference. The plan is freed when unreferenced and evicted (or never cached). NULL is a no-op. */
+void wa_plan_release(wa_plan_t* plan);
+
+/*
+ * Host-only: the plan a geometry would get, without touching any device. Fills `info`; when `groups` is not
+ * NULL writes min(n_groups, groups_cap) group rows; when `items` is not NULL writes min(n_items, items_cap)
+ * work items, 8 int64 each: {b*H + h, kind (0 window, 1 global split), q_lo, q_hi, kv0_lo, kv0_hi, kv1_lo,
+ * kv1_hi}. Errors: as wa_plan_create for the arguments; never WA_ERR_OOM/WA_ERR_CUDA.
+ */
+wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, wa_plan_info_t* info,
+                               wa_group_t* groups, int64_t groups_cap, int64_t* items, int64_t items_cap);
+
+/* Static string for a status code ("WA_OK", ...); "WA_UNKNOWN" for other values. */
+const char* wa_status_string(wa_status s);
+
+/* ---- test hooks: not needed in normal use ---------------------------------------------------------------- */
+
+/*
+ * Fault injection for the watchdog test. flags & 1: the next forward's producer skips one key-tile copy, so the
+ * consumer's bounded wait runs out (about 2 s), the kernel unwinds and latches WA_ERR_DEVICE_TIMEOUT, which
+ * wa_plan_check_error() then reports. The device stays usable; later forwards with flags == 0 are correct.
+ * Returns WA_ERR_INVALID for a NULL plan.
+ */
+int wa_plan_set_debug_flags(wa_plan_t* plan, int flags);
+
+/* Number of plans currently held by the cache (referenced or not). */
+int wa_cache_size(void);
+
+/* Reference count of a plan; -1 for NULL. */
+int wa_plan_refcount(const wa_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WA_H_ */

@@ -1,0 +1,82 @@
+"""The C ABI without a GPU: every declared symbol is exported, status strings, and synchronous argument errors
+(which are checked before any device call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "wa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(wa_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(walib):
+    names = declared_functions()
+    assert "wa_forward" in names and "wa_plan_create" in names
+    lib = ctypes.CDLL(walib.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(walib.EXPORTS)
+
+
+def test_status_strings(walib):
+    for code, name in walib.STATUS.items():
+        assert walib.wa_status_string(code) == name
+    assert walib.wa_status_string(99) == "WA_UNKNOWN"
+
+
+BAD = [
+    dict(T=0), dict(S=0), dict(K=0), dict(r=-1), dict(G=-1), dict(B=0), dict(H=0), dict(global_pos=2),
+    dict(strides=(8, 8, 8)),            # overlapping rows
+    dict(strides=(4096 * 2, 128, 12)),  # stride not a multiple of 8 elements
+    dict(strides=(0, 128, 128)),
+]
+
+
+@pytest.mark.parametrize("bad", BAD)
+def test_invalid_geometry_is_rejected_synchronously(walib, bad):
+    a = dict(T=4, S=8, K=2, r=1, G=3, B=1, H=1, D=128, global_pos=0, strides=None)
+    a.update(bad)
+    L = a["T"] * a["S"] + a["G"]
+    lay = walib.make_layout(a["B"], L, a["H"], a["D"], a["global_pos"], a["strides"])
+    lib = walib.lib()
+    h = ctypes.c_void_p()
+    st = lib.wa_plan_create(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), ctypes.byref(h))
+    assert st == 1 and not h.value
+    info = walib.wa_plan_info_t()
+    assert lib.wa_geometry_describe(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), ctypes.byref(info),
+                                    None, 0, None, 0) == 1
+
+
+def test_unsupported_head_dim(walib):
+    lib = walib.lib()
+    for D in (32, 96, 256):
+        lay = walib.make_layout(1, 35, 1, D, 0)
+        h = ctypes.c_void_p()
+        assert lib.wa_plan_create(4, 8, 2, 1, 3, ctypes.byref(lay), ctypes.byref(h)) == 2
+
+
+def test_null_arguments(walib):
+    lib = walib.lib()
+    lay = walib.make_layout(1, 35, 1, 128, 0)
+    assert lib.wa_plan_create(4, 8, 2, 1, 3, None, ctypes.byref(ctypes.c_void_p())) == 1
+    assert lib.wa_plan_create(4, 8, 2, 1, 3, ctypes.byref(lay), None) == 1
+    assert lib.wa_forward(None, None, None, None, None, None) == 1
+    assert lib.wa_plan_check_error(None, None) == 1
+    assert lib.wa_plan_info(None, None) == 1
+    lib.wa_plan_release(None)  # no-op
+    assert lib.wa_plan_refcount(None) == -1
+    assert lib.wa_plan_set_debug_flags(None, 1) == 1
+
+
+def test_describe_without_device(walib):
+    lay = walib.make_layout(1, 104, 2, 64, 0)
+    info, groups, items = walib.wa_geometry_describe(6, 16, 2, 1, 8, lay, with_items=True)
+    assert info["n_groups"] == 3 and len(groups) == 3
+    assert info["kept_pairs"] == 8768
+    assert len(items) == info["n_items"]
