@@ -1,0 +1,343 @@
+#!/usr/bin/env python3
+"""Throughput of chunk-aligned window softmax attention on GB300: kept-pair TFLOP/s and ms per layer call.
+
+One step = one ``wa_forward`` call (the persistent attention kernel over every window and global-split tile, then
+the log-sum-exp merge of the global rows) on the H3-scale layer: B=1, H=56, D=128, T=102 latent frames of S=960
+tokens, chunks of K=3 frames, radius r=1, G=2048 global tokens after the frames (L=99,968), keys of the global
+rows scaled x2. Useful work counts only kept (query, key) pairs: 4*D flops per pair.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload h3|medium|ragged|tiny|sweep_T..] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the layer on its own GPU (no data exchange; the path is
+replicated, not sharded) and rank 0 prints one JSON line with the whole-job throughput over the slowest rank.
+``--impl reference`` times the CPU oracle on the host cores instead (rank 0 only), on a bounded row sample.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "kept-pair TFLOP/s and ms/call (1×GB300), % of dense BF16 tensor peak"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "window_attention_kernel_h3.md")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="h3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def workload(name):
+    from chunk_windowed_softmax_gb300 import configs
+    if name in configs.ALL:
+        return configs.ALL[name]
+    for w in configs.sweep():
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}")
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": f"{w.name}: B={w.B} H={w.H} D={w.D} T={w.T} S={w.S} K={w.K} r={w.r} G={w.G} "
+                       f"globals={'front' if w.global_pos else 'back'} L={w.L}",
+           "B": w.B, "H": w.H, "D": w.D, "T": w.T, "S": w.S, "K": w.K, "r": w.r, "G": w.G, "L": w.L,
+           "global_pos": "front" if w.global_pos else "back", "k_global_scale": w.k_global_scale,
+           "parallelism": "replicas"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p["bf16_tflops"], p.get("bf16_tflops_sustained"), p["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def stored_traffic():
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if the kernel source it
+    was taken on is the current one (else None)."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, "chunk_windowed_softmax_gb300", "csrc", "wa_kernels.cu"), "rb").read()
+        digest = hashlib.sha256(src).hexdigest()[:16]
+        fields = {}
+        for line in open(PROFILE_SUMMARY):
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+        if fields.get("kernel source sha256[:16]") != digest:
+            return None
+        return float(fields["dram bytes per full H3 launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self, t0, t1):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = []
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+            except Exception:
+                continue
+        os.unlink(self.f.name)
+        sel = [r for r in rows if t0 - 1 <= r[0] <= t1 + 1] or rows
+        if not sel:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in sel for n, a in zip(names, r[3]) if a.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel)}
+
+
+def oracle_sample(w, q, k, v, heads, chunks, global_rows):
+    """Run the CPU oracle on a row sample; returns (seconds, kept-pair flops of the sample, rows)."""
+    import oracle.ref as ref
+    flops = 0.0
+    t0 = time.perf_counter()
+    nrows = 0
+    for h in heads:
+        frames = [t for c in chunks for t in ref.chunk_frames(c, w.T, w.K)]
+        res = ref.window_attention_rows(q, k, v, w.T, w.S, w.K, w.r, w.G, w.global_pos, 0, h, frames=frames,
+                                        global_rows=False)
+        nrows += len(res)
+        for t in frames:
+            flops += 4.0 * w.D * w.S * len(ref.kept_set_of_frame(t, w.T, w.S, w.K, w.r, w.G, w.global_pos))
+        if global_rows and w.G:
+            sub = ref.window_attention_rows(q, k, v, w.T, w.S, w.K, w.r, w.G, w.global_pos, 0, h, frames=[],
+                                            global_rows=True)
+            nrows += len(sub)
+            flops += 4.0 * w.D * w.G * w.L
+    return time.perf_counter() - t0, flops, nrows
+
+
+def host_inputs(w):
+    """q, k, v on the host (drawn on the GPU when there is one: the same generator the GPU arm uses)."""
+    import torch
+    from chunk_windowed_softmax_gb300 import inputs
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    return tuple(t.cpu() for t in inputs.make_qkv(w, device=dev))
+
+
+def cores_used():
+    n = len(os.sched_getaffinity(0))
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            n = min(n, int(os.environ[var]))
+    return n
+
+
+def run_reference(args, w, rank):
+    """The CPU oracle, as it stands, on the host cores: each step a bounded row sample of the workload."""
+    if rank != 0:
+        return
+    import oracle.ref as ref
+    q, k, v = host_inputs(w)
+    nc = ref.num_chunks(w.T, w.K)
+
+    def step(i):
+        h = i % w.H
+        c = (i * 7) % nc
+        return oracle_sample(w, q, k, v, heads=[h], chunks=[c], global_rows=False)
+
+    for i in range(args.warmup):
+        step(i)
+    tot_s, tot_f = 0.0, 0.0
+    for i in range(args.steps):
+        s, f, _ = step(args.warmup + i)
+        tot_s += s
+        tot_f += f
+    value = tot_f / tot_s / 1e12
+    sample = (f"per step: every row of one chunk ({w.K * w.S} rows) of one head, cycling heads and chunks; "
+              f"{args.steps} steps")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, {"timed": "CPU oracle (numpy float64) on a row sample per step"}),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import chunk_windowed_softmax_gb300 as wa
+    from chunk_windowed_softmax_gb300 import _build, inputs
+    _build.build()
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    q, k, v = inputs.make_qkv(w, device=dev)
+    plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    info = plan.info()
+    flops = 4.0 * w.D * info["kept_pairs"] * w.B * w.H
+    launches_per_step = 1 + (1 if w.G > 0 else 0)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        plan.forward(q, k, v, out=out)
+    st = plan.check_error()
+    if st != 0:
+        raise SystemExit(f"device error during warm-up: {wa.wa_status_string(st)}")
+
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        gpu_index = vis.split(",")[local]
+    sampler = ClockSampler(gpu_index)
+    time.sleep(0.3)
+    plan.profile(True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        plan.forward(q, k, v, out=out)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t1 = time.time()
+    ms = e0.elapsed_time(e1) / args.steps
+    attn_ms, comb_ms, nrec = plan.profile_read()
+    plan.profile(False)
+    clocks = sampler.stop(t0, t1)
+    st = plan.check_error()
+    if st != 0:
+        raise SystemExit(f"device error during the timed steps: {wa.wa_status_string(st)}")
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    attn_avg = attn_ms / max(1, nrec)
+    bf16_peak, bf16_sus, hbm, peak_kind = peaks()
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+
+    # End to end through the public call with host tensors: pinned host -> device copies, the forward, and the
+    # device -> host copy of the result, every step.
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    del out
+    wa.forward(qh, kh, vh, w.T, w.S, w.K, w.r, w.G, w.global_pos, out=oh)
+    barrier()
+    torch.cuda.synchronize(dev)
+    tt0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        wa.forward(qh, kh, vh, w.T, w.S, w.K, w.r, w.G, w.global_pos, out=oh)
+    torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - tt0) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * flops / e2e_s / 1e12
+    nbytes = q.numel() * q.element_size()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        qc, kc, vc = qh, kh, vh
+        import oracle.ref as ref
+        nc = ref.num_chunks(w.T, w.K)
+        heads = sorted({0, w.H // 2, w.H - 1})
+        chunks = sorted({0, nc // 2, nc - 1})
+        s, f, nrows = oracle_sample(w, qc, kc, vc, heads, chunks, global_rows=True)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+               "sample": f"heads {heads}: all {w.G} global rows + every row of chunks {chunks} ({nrows} rows, "
+                         f"{f / 1e12:.3f} kept TFLOP, {s:.1f} s); throughput of the sample"}
+
+    if rank == 0:
+        traffic = stored_traffic()
+        res = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w, {"l2": f"no flush: q, k, v ({3 * nbytes / 1e9:.2f} GB read per step) are "
+                                                f"far larger than the 129 MB L2",
+                                          "kept_pairs_per_head": info["kept_pairs"],
+                                          "kept_tflop_per_step": flops / 1e12}),
+            "pct_of_bf16_peak": 100.0 * value / world / bf16_peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": achieved / bf16_peak, "traffic": traffic,
+                         "kernel": f"window_attention_kernel<{w.D}>", "kernel_ms": attn_avg,
+                         "merge_kernel_ms": comb_ms / max(1, nrec),
+                         "peak_kind": f"{peak_kind} bf16 burst (sustained {bf16_sus})"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * nbytes,
+                    "d2h_bytes_per_step": nbytes, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(res), flush=True)
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

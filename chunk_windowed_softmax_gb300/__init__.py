@@ -17,7 +17,8 @@ STATUS = {0: "WA_OK", 1: "WA_ERR_INVALID", 2: "WA_ERR_UNSUPPORTED", 3: "WA_ERR_O
 
 # Symbols declared in include/wa.h (the tests check that the library exports each of them).
 EXPORTS = ("wa_plan_create", "wa_forward", "wa_plan_check_error", "wa_plan_info", "wa_plan_release",
-           "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount")
+           "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount",
+           "wa_plan_profile", "wa_plan_profile_read")
 
 
 class WAError(RuntimeError):
@@ -76,6 +77,11 @@ def lib():
         L.wa_status_string.restype = ctypes.c_char_p
         L.wa_plan_set_debug_flags.argtypes = [P, ctypes.c_int]
         L.wa_plan_set_debug_flags.restype = ctypes.c_int
+        L.wa_plan_profile.argtypes = [P, ctypes.c_int]
+        L.wa_plan_profile.restype = ctypes.c_int
+        L.wa_plan_profile_read.argtypes = [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_int)]
+        L.wa_plan_profile_read.restype = ctypes.c_int
         L.wa_cache_size.argtypes = []
         L.wa_cache_size.restype = ctypes.c_int
         L.wa_plan_refcount.argtypes = [P]
@@ -179,6 +185,17 @@ class Plan:
         import torch
         s = torch.cuda.current_stream() if stream is None else stream
         return wa_plan_check_error(self.handle, s.cuda_stream)
+
+    def profile(self, enable=True):
+        """Start (or stop) recording per-kernel device times of this plan's forwards."""
+        _check(lib().wa_plan_profile(self.handle, 1 if enable else 0), "wa_plan_profile")
+
+    def profile_read(self):
+        """(attention kernel ms, merge kernel ms, forwards) summed over the recorded forwards."""
+        a, c, n = ctypes.c_double(), ctypes.c_double(), ctypes.c_int()
+        _check(lib().wa_plan_profile_read(self.handle, ctypes.byref(a), ctypes.byref(c), ctypes.byref(n)),
+               "wa_plan_profile_read")
+        return a.value, c.value, n.value
 
     def set_debug_flags(self, flags):
         _check(lib().wa_plan_set_debug_flags(self.handle, flags), "wa_plan_set_debug_flags")

@@ -6,11 +6,16 @@
 // VDN-Minimax-H3 window-attention article, section 三: every kept (query, key) pair lies in a dense rectangle,
 // and each rectangle is computed as plain dense attention with no mask except at segment tails.
 //
-// CTA roles (320 threads, one CTA per SM):
-//   warps 0-3  softmax warpgroup of query tile 0: one thread per query row / TMEM lane
-//   warps 4-7  softmax warpgroup of query tile 1
-//   warp 8     MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V with tcgen05.mma, accumulators in TMEM
-//   warp 9     TMA producer (one thread): Q tiles and a ring of K / V tiles, 128-byte swizzled
+// CTA roles (384 threads = 3 warpgroups, one CTA per SM):
+//   warps 0-3   softmax warpgroup of query tile 0: one thread per query row / TMEM lane
+//   warps 4-7   softmax warpgroup of query tile 1
+//   warp 8      MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V with tcgen05.mma, accumulators in TMEM
+//   warp 9      TMA producer (one thread): Q tiles and a ring of K / V tiles, 128-byte swizzled
+//   warps 10-11 idle
+// The launch gives every thread 168 registers (384 x 168 = 64512); setmaxnreg then moves them to where the work
+// is: the softmax warpgroups rise to 200 (a full 128-column score row stays in registers), the third warpgroup
+// drops to 104. 2 x 128 x 200 + 128 x 104 = 64512, the launch's total. Each role branch ends with its own copy of
+// the teardown, so that no code is shared by regions with different register counts.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [384, 384+D). P_t (bf16) overwrites the
 // first 64 columns of S_t and is the A operand of the P.V MMA, read straight from TMEM.
 // The two query tiles ping-pong: while one warpgroup runs the softmax of its tile, the tensor core works on the
@@ -34,9 +39,12 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+constexpr uint32_t kSoftmaxRegs = 200;
+constexpr uint32_t kControlRegs = 104;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split exceeds the launch");
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O only when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms: waiting for in-flight copies while unwinding
@@ -148,7 +156,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   int* err = prm.err;
 
-  if (warp == kLoadWarp) {
+  auto teardown = [&]() {  // every thread: wait for all roles, then warp 0 frees the tensor memory
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+      __syncwarp();  // tcgen05.dealloc is warp-collective: reconverge after the role branches
+      tmem_dealloc(tmem, 512);
+    }
+  };
+
+  if (warp >= 8) {
+    regs_dec<kControlRegs>();
+    if (warp == kLoadWarp) {
     // ------------------------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t kv_n = 0;
@@ -202,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_n1) mbar_wait_drain(bars.q_full(1), (q_n1 - 1) & 1, kDrainLimitNs);
       }
     }
-  } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t kv_n = 0;
@@ -297,7 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bars.drain());
       mbar_wait_drain(bars.drain(), 0, ok ? kWaitLimitNs : kDrainLimitNs);
     }
+    }
+    teardown();
   } else {
+    regs_inc<kSoftmaxRegs>();
     // ---------------------------------------------------------------------------------- softmax warpgroups
     const int t = warp >> 2;            // query tile of this warpgroup
     const int row_in_tile = tid & 127;  // == TMEM lane
@@ -339,23 +362,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx3 = fmaxf(mx3, s[c + 3]);
         }
         const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * prm.c_scale;
+        // The running max only moves when it grows by more than 2^8; the O rescale that a move needs is done
+        // after P is written (it does not need the scores, so the score row is dead by then).
+        float alpha = 1.f;
+        bool rescale = false;
         if (j == 0) {
           m = m_cand;
         } else {
           const bool need = m_cand > m + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2(m - m_cand) : 1.f;
-            if (need) m = m_cand;
-            l *= alpha;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t o[32];
-              tmem_ld_x32(tO + c0, o);
-#pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              tmem_st_x32(tO + c0, o);
-            }
-            tmem_wait_st();
+          rescale = __any_sync(0xffffffffu, need);
+          if (need) {
+            alpha = ex2(m - m_cand);
+            m = m_cand;
           }
         }
         const float neg_m = -m;
@@ -374,7 +392,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st_x32(tS + 32 * half, pk);
         }
-        l += sum0 + sum1;
+        l = l * alpha + (sum0 + sum1);
+        if (rescale) {  // warp-uniform: tcgen05.ld/st are warp-collective
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + c0, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st_x32(tO + c0, o);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_p);
@@ -429,14 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) {
-    __syncwarp();  // tcgen05.dealloc is warp-collective: reconverge after the role branches
-    tmem_dealloc(tmem, 512);
+    teardown();
   }
 }
 

@@ -31,6 +31,11 @@ struct wa_plan {
   bool have_last = false;
   cudaEvent_t done = nullptr;
   int debug_flags = 0;
+  // Launch timing (wa_plan_profile): three events per forward, recorded on the forward's stream before the
+  // attention kernel, between the two kernels and after the merge kernel.
+  bool profiling = false;
+  int prof_n = 0;
+  std::vector<cudaEvent_t> prof_ev;
 };
 
 namespace wa {
@@ -184,6 +189,7 @@ void free_plan(wa_plan* p) {
   if (p->d_ws) cudaFree(p->d_ws);
   if (p->d_err) cudaFree(p->d_err);
   if (p->done) cudaEventDestroy(p->done);
+  for (cudaEvent_t e : p->prof_ev) cudaEventDestroy(e);
   if (p->device >= 0 && cur >= 0 && cur != p->device) cudaSetDevice(cur);
   delete p;
 }
@@ -238,6 +244,8 @@ wa_status create_uncached(const wa::Geometry& g, int dev, wa_plan** out) {
   *out = p;
   return WA_OK;
 }
+
+constexpr int kMaxProfiled = 4096;
 
 bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) { return a < b + nb && b < a + na; }
 
@@ -379,11 +387,46 @@ wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* 
   a.n_splits = plan->hp.n_splits;
   a.debug_flags = plan->debug_flags;
   a.geo = &g;
+  cudaEvent_t* ev = nullptr;
+  if (plan->profiling && plan->prof_n < kMaxProfiled) {
+    while ((int)plan->prof_ev.size() < 3 * (plan->prof_n + 1)) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return WA_ERR_CUDA;
+      plan->prof_ev.push_back(e);
+    }
+    ev = &plan->prof_ev[3 * plan->prof_n++];
+  }
+  if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) return WA_ERR_CUDA;
   if (a.n_items > 0 && wa::launch_attention(a, (void*)s, plan->num_sms) != 0) return WA_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[1], s) != cudaSuccess) return WA_ERR_CUDA;
   if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[2], s) != cudaSuccess) return WA_ERR_CUDA;
   if (cudaEventRecord(plan->done, s) != cudaSuccess) return WA_ERR_CUDA;
   plan->last_stream = s;
   plan->have_last = true;
+  return WA_OK;
+}
+
+int wa_plan_profile(wa_plan_t* plan, int enable) {
+  if (!plan) return WA_ERR_INVALID;
+  plan->profiling = enable != 0;
+  plan->prof_n = 0;
+  return WA_OK;
+}
+
+int wa_plan_profile_read(wa_plan_t* plan, double* attention_ms, double* combine_ms, int* n_forwards) {
+  if (!plan || !attention_ms || !combine_ms || !n_forwards) return WA_ERR_INVALID;
+  *attention_ms = *combine_ms = 0.0;
+  *n_forwards = plan->prof_n;
+  for (int i = 0; i < plan->prof_n; ++i) {
+    cudaEvent_t* ev = &plan->prof_ev[3 * i];
+    float a = 0.f, c = 0.f;
+    if (cudaEventSynchronize(ev[2]) != cudaSuccess || cudaEventElapsedTime(&a, ev[0], ev[1]) != cudaSuccess ||
+        cudaEventElapsedTime(&c, ev[1], ev[2]) != cudaSuccess)
+      return WA_ERR_CUDA;
+    *attention_ms += a;
+    *combine_ms += c;
+  }
   return WA_OK;
 }
 

@@ -136,6 +136,16 @@ const char* wa_status_string(wa_status s);
  */
 int wa_plan_set_debug_flags(wa_plan_t* plan, int flags);
 
+/*
+ * Launch timing. enable != 0 starts recording (and clears earlier records): each later wa_forward on the plan
+ * records CUDA events on its stream before the attention kernel, between the two kernels and after the merge
+ * kernel (up to 4096 forwards). wa_plan_profile_read() waits for the recorded events and returns the summed
+ * device time of each kernel in milliseconds and the number of forwards recorded. Returns WA_ERR_INVALID for
+ * NULL arguments, WA_ERR_CUDA if an event call fails.
+ */
+int wa_plan_profile(wa_plan_t* plan, int enable);
+int wa_plan_profile_read(wa_plan_t* plan, double* attention_ms, double* combine_ms, int* n_forwards);
+
 /* Number of plans currently held by the cache (referenced or not). */
 int wa_cache_size(void);
 

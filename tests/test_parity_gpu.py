@@ -101,9 +101,9 @@ def test_strided_layouts(cuda, kind):
 
 def sampled_compare(wa, w, heads, chunks, bench_launch=True):
     """Full-size workload in the benchmark's launch configuration; the oracle computes a row sample."""
-    q, k, v = inputs.make_qkv(w)
     dev = torch.device("cuda")
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    qd, kd, vd = inputs.make_qkv(w, device=dev)
+    q, k, v = qd.cpu(), kd.cpu(), vd.cpu()
     plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
     try:
         out = plan.forward(qd, kd, vd)
@@ -157,7 +157,7 @@ def test_window_rows_ignore_keys_outside_window(cuda):
     """At full H3 size: changing every key and value outside chunk 0's window leaves chunk 0's rows bit-identical,
     and changes the global rows (they see everything)."""
     w = configs.H3
-    q, k, v = (t.cuda() for t in inputs.make_qkv(w))
+    q, k, v = inputs.make_qkv(w, device="cuda")
     plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
     try:
         a = plan.forward(q, k, v)
