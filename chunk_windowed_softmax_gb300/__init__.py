@@ -18,7 +18,7 @@ STATUS = {0: "WA_OK", 1: "WA_ERR_INVALID", 2: "WA_ERR_UNSUPPORTED", 3: "WA_ERR_O
 # Symbols declared in include/wa.h (the tests check that the library exports each of them).
 EXPORTS = ("wa_plan_create", "wa_forward", "wa_plan_check_error", "wa_plan_info", "wa_plan_release",
            "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount",
-           "wa_plan_profile", "wa_plan_profile_read")
+           "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static")
 
 
 class WAError(RuntimeError):
@@ -82,6 +82,8 @@ def lib():
         L.wa_plan_profile_read.argtypes = [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                            ctypes.POINTER(ctypes.c_int)]
         L.wa_plan_profile_read.restype = ctypes.c_int
+        L.wa_forward_static.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(wa_layout_t), P, P, P, P, P]
+        L.wa_forward_static.restype = ctypes.c_int
         L.wa_cache_size.argtypes = []
         L.wa_cache_size.restype = ctypes.c_int
         L.wa_plan_refcount.argtypes = [P]
@@ -117,6 +119,13 @@ def wa_plan_create(T, S, K, r, G, layout):
 def wa_forward(plan, q_ptr, k_ptr, v_ptr, out_ptr, stream_ptr):
     _check(lib().wa_forward(plan, ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                             ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream_ptr)), "wa_forward")
+
+
+def wa_forward_static(T, S, K, r, G, layout, q_ptr, k_ptr, v_ptr, out_ptr, stream_ptr):
+    """Forward pass with no device allocation (library-owned static scratch); raises WAError on failure."""
+    _check(lib().wa_forward_static(T, S, K, r, G, ctypes.byref(layout), ctypes.c_void_p(q_ptr),
+                                   ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr), ctypes.c_void_p(out_ptr),
+                                   ctypes.c_void_p(stream_ptr)), "wa_forward_static")
 
 
 def wa_plan_check_error(plan, stream_ptr):

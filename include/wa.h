@@ -126,6 +126,28 @@ wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layou
 /* Static string for a status code ("WA_OK", ...); "WA_UNKNOWN" for other values. */
 const char* wa_status_string(wa_status s);
 
+/*
+ * The same forward pass as wa_forward, for callers that may not allocate device memory (the article has no
+ * counterpart to this entry point). Such callers include frameworks that hand out device memory only from their
+ * own accounted pool, processes under a fixed device-memory budget, and code that must avoid the device-wide
+ * synchronisation cudaMalloc / cudaFree can cause. It needs no plan: the work list, the global-leg workspace and
+ * the device error word live in one library-owned 32 MiB __device__ array that exists on every GPU where the
+ * library's device code is loaded, until the process exits. It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *   Arguments: as wa_plan_create (geometry, layout) plus q, k, v, out and stream as wa_forward. The work list is
+ *   rebuilt on the host and copied from ordinary host memory into the array on every call.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ *   current; make that first call before any stream capture.
+ *   Every call shares the one array: calls that overlap on the GPU (different streams or threads) race on it;
+ *   calls on one stream are ordered. The array keeps the previous call's contents; the call clears what must
+ *   start at zero.
+ * Errors: as wa_forward; WA_ERR_UNSUPPORTED, before anything is launched, when the geometry's scratch (work list
+ * + B*H*G*n_splits*(D+1)*4 bytes of workspace) exceeds the 32 MiB array. Device-side watchdog failures are latched
+ * in the array's error word and cleared by the next call; this entry point does not report them.
+ */
+wa_status wa_forward_static(int T, int S, int K, int r, int G, const wa_layout_t* layout, const void* q,
+                            const void* k, const void* v, void* out, wa_stream_t stream);
+
 /* ---- test hooks: not needed in normal use ---------------------------------------------------------------- */
 
 /*

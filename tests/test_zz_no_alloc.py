@@ -1,0 +1,71 @@
+"""wa_forward_static: the forward pass for callers that may not allocate device memory (for example a framework
+that only hands out memory from its own accounted pool, or code under a fixed device-memory budget). Its scratch
+is a library-owned static device array, so it is checked here against the plan-based wa_forward on the same
+inputs, on two calls in a row with different geometries, so that a stale scratch from the first call cannot
+leak into the second. Named to be collected last."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from chunk_windowed_softmax_gb300 import configs, inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 5e-3
+ABS_TOL = 3e-2
+
+
+def static_forward(wa, w, q, k, v):
+    out = torch.empty_like(q)
+    lay = wa.make_layout(w.B, w.L, w.H, w.D, w.global_pos)
+    s = torch.cuda.current_stream().cuda_stream
+    st = wa.lib().wa_forward_static(w.T, w.S, w.K, w.r, w.G, ctypes.byref(lay), ctypes.c_void_p(q.data_ptr()),
+                                    ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+                                    ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(s))
+    assert st == 0, wa.wa_status_string(st)
+    torch.cuda.synchronize()
+    return out
+
+
+def plan_forward(wa, w, q, k, v):
+    plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    try:
+        out = plan.forward(q, k, v)
+        assert plan.check_error() == 0
+    finally:
+        plan.close()
+    return out
+
+
+def close(a, b):
+    a, b = a.float().cpu().numpy(), b.float().cpu().numpy()
+    for bi in range(a.shape[0]):
+        for h in range(a.shape[2]):
+            x, y = a[bi, :, h], b[bi, :, h]
+            assert np.linalg.norm(x - y) / np.linalg.norm(y) <= REL_TOL
+            assert np.abs(x - y).max() <= ABS_TOL
+
+
+def test_static_scratch_matches_plan_forward_twice(cuda):
+    for w in (configs.MEDIUM, configs.RAGGED):  # two calls in a row, different geometries and scratch layouts
+        q, k, v = inputs.make_qkv(w, device="cuda")
+        close(static_forward(cuda, w, q, k, v), plan_forward(cuda, w, q, k, v))
+    w = configs.MEDIUM  # and once more on the first geometry, over the second call's leftover scratch
+    q, k, v = inputs.make_qkv(w, seed=77, device="cuda")
+    close(static_forward(cuda, w, q, k, v), plan_forward(cuda, w, q, k, v))
+
+
+def test_static_scratch_rejects_oversized_geometry(cuda):
+    # 200,000 global rows: the global-leg workspace alone exceeds the 32 MiB array; nothing may be launched
+    T, S, K, r, G = 1, 8, 1, 0, 200000
+    L = T * S + G
+    q = torch.zeros(1, L, 1, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    lay = cuda.make_layout(1, L, 1, 128, 0)
+    st = cuda.lib().wa_forward_static(T, S, K, r, G, ctypes.byref(lay), ctypes.c_void_p(q.data_ptr()),
+                                      ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(q.data_ptr()),
+                                      ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(0))
+    assert st == 2  # WA_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
