@@ -353,15 +353,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= valid) s[c] = -INFINITY;
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // Row max: 8 independent chains of three-input maxima over 16 columns each.
+        float mx[8];
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int a = 0; a < 8; ++a) {
+          mx[a] = fmaxf(s[16 * a], s[16 * a + 15]);
+#pragma unroll
+          for (int c = 1; c < 15; c += 2) mx[a] = max3(mx[a], s[16 * a + c], s[16 * a + c + 1]);
         }
-        const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * prm.c_scale;
+        const float m_cand =
+            fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7])) * prm.c_scale;
         // The running max only moves when it grows by more than 2^8; the O rescale that a move needs is done
         // after P is written (it does not need the scores, so the score row is dead by then).
         float alpha = 1.f;
@@ -377,22 +378,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float neg_m = -m;
-        float sum0 = 0.f, sum1 = 0.f;
+        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 4 independent pairs: short add chains
 #pragma unroll
         for (int half = 0; half < 2; ++half) {  // P(bf16) for 64 key columns -> 32 TMEM columns over S
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2(fmaf(s[64 * half + 2 * c], prm.c_scale, neg_m));
-            const float p1 = ex2(fmaf(s[64 * half + 2 * c + 1], prm.c_scale, neg_m));
-            sum0 += p0;
-            sum1 += p1;
+            float x0, x1;
+            fma2(x0, x1, s[64 * half + 2 * c], s[64 * half + 2 * c + 1], prm.c_scale, prm.c_scale, neg_m, neg_m);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            add2(sum[2 * (c & 3)], sum[2 * (c & 3) + 1], sum[2 * (c & 3)], sum[2 * (c & 3) + 1], p0, p1);
             __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
             pk[c] = *reinterpret_cast<uint32_t*>(&v2);
           }
           tmem_st_x32(tS + 32 * half, pk);
         }
-        l = l * alpha + (sum0 + sum1);
+        l = l * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
         if (rescale) {  // warp-uniform: tcgen05.ld/st are warp-collective
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {

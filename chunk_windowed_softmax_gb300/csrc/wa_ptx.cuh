@@ -166,6 +166,38 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pairs of fp32 operations (one instruction for two lanes of work on sm_100+).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+  asm("{\n"
+      "  .reg .b64 ra, rb, rc, rd;\n"
+      "  mov.b64 ra, {%2, %3};\n"
+      "  mov.b64 rb, {%4, %5};\n"
+      "  mov.b64 rc, {%6, %7};\n"
+      "  fma.rn.f32x2 rd, ra, rb, rc;\n"
+      "  mov.b64 {%0, %1}, rd;\n"
+      "}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n"
+      "  .reg .b64 ra, rb, rd;\n"
+      "  mov.b64 ra, {%2, %3};\n"
+      "  mov.b64 rb, {%4, %5};\n"
+      "  add.rn.f32x2 rd, ra, rb;\n"
+      "  mov.b64 {%0, %1}, rd;\n"
+      "}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
