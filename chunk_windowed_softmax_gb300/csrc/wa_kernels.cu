@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.q_full(t), 1);
       mbar_init(bars.q_empty(t), 1);
       mbar_init(bars.s_full(t), 1);
-      mbar_init(bars.p_full(t), 128);
+      mbar_init(bars.p_full(t), 4);  // one arrive per softmax warp
       mbar_init(bars.o_full(t), 1);
     }
     mbar_init(bars.drain(), 1);
@@ -228,21 +228,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kv_n = 0;
       uint32_t q_n0 = 0, q_n1 = 0, p_n0 = 0, p_n1 = 0;
       bool ok = true;
-      // O_t (+)= P_t V, P_t read from TMEM (aliasing S_t), V from the ring slot at `vaddr` (MN-major: D contiguous)
-      auto issue_pv = [&](int t, uint32_t vaddr, bool acc_first) {
+      // Descriptors are built once; a shared-memory offset is added to the start-address field (address >> 4,
+      // 14 bits: every address of the 227 KB window fits, so the addition never carries out of the field).
+      const uint64_t dq = sdesc_sw128(sQ, 16, 1024);                 // Q tiles, K-major
+      const uint64_t dk = sdesc_sw128(sKV, 16, 1024);                // K tiles, K-major
+      const uint64_t dv = sdesc_sw128(sKV, C::kHalfBytes, 1024);     // V tiles, MN-major (D contiguous)
+      // O_t (+)= P_t V, P_t read from TMEM (aliasing S_t), V from ring slot `vslot`
+      auto issue_pv = [&](int t, uint32_t vslot, bool acc_first) {
+        const uint64_t d0 = dv + ((vslot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_ts(tmem + C::kTmemO + t * 128, tmem + t * 128 + kk * 8,
-                 sdesc_sw128(vaddr + kk * 2048, C::kHalfBytes, 1024), C::kIdescPV, (acc_first || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kTmemO + t * 128, tmem + t * 128 + kk * 8, d0 + ((kk * 2048) >> 4), C::kIdescPV,
+                 (acc_first || kk > 0) ? 1u : 0u);
       };
       // S_t = Q_t K^T, both K-major; K = D advances 32 bytes inside a 128-byte swizzle row, then to the next box
-      auto issue_s = [&](int t, uint32_t kaddr) {
-        const uint32_t qaddr = sQ + t * C::kTileBytes;
+      auto issue_s = [&](int t, uint32_t kslot) {
+        const uint64_t q0 = dq + ((t * C::kTileBytes) >> 4);
+        const uint64_t k0 = dk + ((kslot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-          mma_ss(tmem + t * 128, sdesc_sw128(qaddr + off, 16, 1024), sdesc_sw128(kaddr + off, 16, 1024), C::kIdescS,
-                 kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk / 4) * C::kHalfBytes + (kk % 4) * 32) >> 4;
+          mma_ss(tmem + t * 128, q0 + off, k0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
@@ -268,8 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && j > 0) ok = mbar_wait(bars.kv_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kaddr = sKV + kslot * C::kTileBytes;
-          const uint32_t vaddr_prev = sKV + prev_vslot * C::kTileBytes;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t >= ntq) break;
@@ -279,9 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               pn++;
               if (!ok) break;
               tc_fence_after();
-              issue_pv(t, vaddr_prev, j > 1);  // O_t += P_t(j-1) V_{j-1}
+              issue_pv(t, prev_vslot, j > 1);  // O_t += P_t(j-1) V_{j-1}
             }
-            issue_s(t, kaddr);  // S_t = Q_t K_j^T
+            issue_s(t, kslot);  // S_t = Q_t K_j^T
             mma_commit(bars.s_full(t));
           }
           if (!ok) break;
@@ -298,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bars.kv_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t vaddr = sKV + prev_vslot * C::kTileBytes;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= ntq) break;
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pn++;
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t, vaddr, nt > 1);
+          issue_pv(t, prev_vslot, nt > 1);
           mma_commit(bars.o_full(t));
         }
         if (!ok) break;
@@ -380,19 +383,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float neg_m = -m;
         float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 4 independent pairs: short add chains
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {  // P(bf16) for 64 key columns -> 32 TMEM columns over S
-          uint32_t pk[32];
+        for (int q4 = 0; q4 < 4; ++q4) {  // P(bf16) for 32 key columns -> 16 TMEM columns over S
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
+          for (int c = 0; c < 16; ++c) {
             float x0, x1;
-            fma2(x0, x1, s[64 * half + 2 * c], s[64 * half + 2 * c + 1], prm.c_scale, prm.c_scale, neg_m, neg_m);
+            fma2(x0, x1, s[32 * q4 + 2 * c], s[32 * q4 + 2 * c + 1], prm.c_scale, prm.c_scale, neg_m, neg_m);
             const float p0 = ex2(x0);
             const float p1 = ex2(x1);
             add2(sum[2 * (c & 3)], sum[2 * (c & 3) + 1], sum[2 * (c & 3)], sum[2 * (c & 3) + 1], p0, p1);
             __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
             pk[c] = *reinterpret_cast<uint32_t*>(&v2);
           }
-          tmem_st_x32(tS + 32 * half, pk);
+          tmem_st_x16(tS + 16 * q4, pk);
         }
         l = l * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
         if (rescale) {  // warp-uniform: tcgen05.ld/st are warp-collective
@@ -407,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_p);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p);
       }
       if (!ok) break;
       ok = mbar_wait(bar_o, o_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
