@@ -54,12 +54,16 @@ struct Cfg {
   static constexpr int kHalves = D / 64;              // 128-byte swizzle boxes per row
   static constexpr int kHalfBytes = kTileRows * 128;  // one box: 128 rows x 64 bf16
   static constexpr int kTileBytes = kTileRows * D * 2;
-  static constexpr int kSlots = D == 128 ? 4 : 8;  // K / V ring
+  // Separate K and V rings; the producer runs K one tile ahead of V (K is needed a step earlier than V).
+  static constexpr int kKSlots = D == 128 ? 3 : 4;
+  static constexpr int kVSlots = D == 128 ? 2 : 4;
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
-  // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain kv_full[kSlots] kv_empty[kSlots]
-  static constexpr int kNumBars = 11 + 2 * kSlots;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kKSlots * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVSlots * kTileBytes;
+  // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain k_full[kKSlots] k_empty[kKSlots]
+  //           v_full[kVSlots] v_empty[kVSlots]
+  static constexpr int kNumBars = 11 + 2 * kKSlots + 2 * kVSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t kTmemO = 256;
@@ -81,7 +85,8 @@ struct Params {
 };
 
 // Shared-memory barrier layout, relative to the barrier block: q_full[2] q_empty[2] s_full[2] p_full[2]
-// o_full[2] drain kv_full[kSlots] kv_empty[kSlots]. Addresses are computed, never indexed from a local array.
+// o_full[2] drain, then the K and V ring barriers. Addresses are computed, never indexed from a local array.
+template <int KS, int VS>
 struct BarAddr {
   uint32_t base;
   __device__ __forceinline__ uint32_t q_full(int t) const { return base + 8 * (0 + t); }
@@ -90,9 +95,10 @@ struct BarAddr {
   __device__ __forceinline__ uint32_t p_full(int t) const { return base + 8 * (6 + t); }
   __device__ __forceinline__ uint32_t o_full(int t) const { return base + 8 * (8 + t); }
   __device__ __forceinline__ uint32_t drain() const { return base + 8 * 10; }
-  __device__ __forceinline__ uint32_t kv_full(uint32_t slot) const { return base + 8 * (11 + slot); }
-  template <int kSlots>
-  __device__ __forceinline__ uint32_t kv_empty(uint32_t slot) const { return base + 8 * (11 + kSlots + slot); }
+  __device__ __forceinline__ uint32_t k_full(uint32_t slot) const { return base + 8 * (11 + slot); }
+  __device__ __forceinline__ uint32_t k_empty(uint32_t slot) const { return base + 8 * (11 + KS + slot); }
+  __device__ __forceinline__ uint32_t v_full(uint32_t slot) const { return base + 8 * (11 + 2 * KS + slot); }
+  __device__ __forceinline__ uint32_t v_empty(uint32_t slot) const { return base + 8 * (11 + 2 * KS + VS + slot); }
 };
 
 __device__ __forceinline__ Item load_item(const Item* items, int idx) {
@@ -103,6 +109,28 @@ __device__ __forceinline__ Item load_item(const Item* items, int idx) {
 
 __device__ __forceinline__ int seg_tiles(int lo, int hi) { return hi > lo ? (hi - lo + kTileRows - 1) / kTileRows : 0; }
 
+// Exponentiate one 128-column score row into bf16 P (written to TMEM over the row's S columns, 16 columns per
+// store) and return the fp32 row sum.
+__device__ __forceinline__ float exp_store_row(const float (&s)[128], float c_scale, float neg_m, uint32_t tS) {
+  float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 4 independent pairs: short add chains
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float x0, x1;
+      fma2(x0, x1, s[32 * q4 + 2 * c], s[32 * q4 + 2 * c + 1], c_scale, c_scale, neg_m, neg_m);
+      const float p0 = ex2(x0);
+      const float p1 = ex2(x1);
+      add2(sum[2 * (c & 3)], sum[2 * (c & 3) + 1], sum[2 * (c & 3)], sum[2 * (c & 3) + 1], p0, p1);
+      __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+      pk[c] = *reinterpret_cast<uint32_t*>(&v2);
+    }
+    tmem_st_x16(tS + 16 * q4, pk);
+  }
+  return ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     window_attention_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -112,13 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sQ = s_base + C::kQOff;
-  const uint32_t sKV = s_base + C::kKVOff;
+  const uint32_t sK = s_base + C::kKOff;
+  const uint32_t sV = s_base + C::kVOff;
   const uint32_t bar0 = s_base + C::kBarOff;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
-  const BarAddr bars{bar0};
-  auto kv_empty = [&](uint32_t slot) { return bars.kv_empty<C::kSlots>(slot); };
+  const BarAddr<C::kKSlots, C::kVSlots> bars{bar0};
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -134,9 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.o_full(t), 1);
     }
     mbar_init(bars.drain(), 1);
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(bars.kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < C::kKSlots; ++s) {
+      mbar_init(bars.k_full(s), 1);
+      mbar_init(bars.k_empty(s), 1);
+    }
+    for (int s = 0; s < C::kVSlots; ++s) {
+      mbar_init(bars.v_full(s), 1);
+      mbar_init(bars.v_empty(s), 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -171,10 +203,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kLoadWarp) {
     // ------------------------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t kv_n = 0;
+      uint32_t k_n = 0, v_n = 0;  // K / V tiles loaded so far (ring slot = n % slots, phase = n / slots)
       uint32_t q_n0 = 0, q_n1 = 0;
       bool dropped = false;
       bool ok = true;
+      // Load one 128-row key or value tile into the next slot of its ring.
+      auto load_kv = [&](bool is_v, int row, int h, int b) -> bool {
+        uint32_t& n = is_v ? v_n : k_n;
+        const uint32_t slots = is_v ? C::kVSlots : C::kKSlots;
+        const uint32_t slot = n % slots;
+        const uint32_t empty = is_v ? bars.v_empty(slot) : bars.k_empty(slot);
+        const uint32_t full = is_v ? bars.v_full(slot) : bars.k_full(slot);
+        if (!mbar_wait(empty, ((n / slots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs)) return false;
+        if ((prm.debug_flags & 1) && !dropped && blockIdx.x == 0) {
+          dropped = true;  // fault injection for the watchdog test: this tile is never loaded
+        } else {
+          mbar_arrive_expect_tx(full, C::kTileBytes);
+          const uint32_t dst = (is_v ? sV : sK) + slot * C::kTileBytes;
+#pragma unroll
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_4d(dst + hf * C::kHalfBytes, is_v ? &tmap_v : &tmap_k, full, hf * 64, h, row, b);
+        }
+        n++;
+        return true;
+      };
       for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
         const Item it = load_item(prm.items, idx);
         const int b = it.bh / prm.H, h = it.bh % prm.H;
@@ -194,30 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
         const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+        auto row_of = [&](int j) { return j < nt0 ? it.s0_lo + j * kTileRows : it.s1_lo + (j - nt0) * kTileRows; };
+        ok = ok && load_kv(false, row_of(0), h, b);
         for (int j = 0; j < nt && ok; ++j) {
-          const int row = j < nt0 ? it.s0_lo + j * kTileRows : it.s1_lo + (j - nt0) * kTileRows;
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            const uint32_t slot = kv_n % C::kSlots;
-            ok = mbar_wait(kv_empty(slot), ((kv_n / C::kSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-            if (!ok) break;
-            if ((prm.debug_flags & 1) && !dropped && blockIdx.x == 0) {
-              dropped = true;  // fault injection for the watchdog test: this tile is never loaded
-            } else {
-              mbar_arrive_expect_tx(bars.kv_full(slot), C::kTileBytes);
-#pragma unroll
-              for (int hf = 0; hf < C::kHalves; ++hf)
-                tma_load_4d(sKV + slot * C::kTileBytes + hf * C::kHalfBytes, which ? &tmap_v : &tmap_k,
-                            bars.kv_full(slot), hf * 64, h, row, b);
-            }
-            kv_n++;
-          }
+          if (j + 1 < nt) ok = load_kv(false, row_of(j + 1), h, b);  // K_{j+1} before V_j
+          ok = ok && load_kv(true, row_of(j), h, b);
         }
       }
       if (!ok) {
         // Unwinding: wait (briefly) for the copies still in flight so that none lands after the CTA exits.
-        for (uint32_t n = kv_n > (uint32_t)C::kSlots ? kv_n - C::kSlots : 0; n < kv_n; ++n)
-          mbar_wait_drain(bars.kv_full(n % C::kSlots), (n / C::kSlots) & 1, kDrainLimitNs);
+        for (uint32_t n = k_n > (uint32_t)C::kKSlots ? k_n - C::kKSlots : 0; n < k_n; ++n)
+          mbar_wait_drain(bars.k_full(n % C::kKSlots), (n / C::kKSlots) & 1, kDrainLimitNs);
+        for (uint32_t n = v_n > (uint32_t)C::kVSlots ? v_n - C::kVSlots : 0; n < v_n; ++n)
+          mbar_wait_drain(bars.v_full(n % C::kVSlots), (n / C::kVSlots) & 1, kDrainLimitNs);
         if (q_n0) mbar_wait_drain(bars.q_full(0), (q_n0 - 1) & 1, kDrainLimitNs);
         if (q_n1) mbar_wait_drain(bars.q_full(1), (q_n1 - 1) & 1, kDrainLimitNs);
       }
@@ -225,14 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t kv_n = 0;
+      uint32_t k_n = 0, v_n = 0;
       uint32_t q_n0 = 0, q_n1 = 0, p_n0 = 0, p_n1 = 0;
       bool ok = true;
       // Descriptors are built once; a shared-memory offset is added to the start-address field (address >> 4,
       // 14 bits: every address of the 227 KB window fits, so the addition never carries out of the field).
       const uint64_t dq = sdesc_sw128(sQ, 16, 1024);                 // Q tiles, K-major
-      const uint64_t dk = sdesc_sw128(sKV, 16, 1024);                // K tiles, K-major
-      const uint64_t dv = sdesc_sw128(sKV, C::kHalfBytes, 1024);     // V tiles, MN-major (D contiguous)
+      const uint64_t dk = sdesc_sw128(sK, 16, 1024);                 // K tiles, K-major
+      const uint64_t dv = sdesc_sw128(sV, C::kHalfBytes, 1024);      // V tiles, MN-major (D contiguous)
       // O_t (+)= P_t V, P_t read from TMEM (aliasing S_t), V from ring slot `vslot`
       auto issue_pv = [&](int t, uint32_t vslot, bool acc_first) {
         const uint64_t d0 = dv + ((vslot * C::kTileBytes) >> 4);
@@ -266,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t prev_vslot = 0, prev_vpar = 0;
         for (int j = 0; j < nt; ++j) {
-          const uint32_t kslot = kv_n % C::kSlots, kpar = (kv_n / C::kSlots) & 1;
-          ++kv_n;
-          const uint32_t vslot = kv_n % C::kSlots, vpar = (kv_n / C::kSlots) & 1;
-          ++kv_n;
-          ok = mbar_wait(bars.kv_full(kslot), kpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
-          if (ok && j > 0) ok = mbar_wait(bars.kv_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          const uint32_t kslot = k_n % C::kKSlots, kpar = (k_n / C::kKSlots) & 1;
+          ++k_n;
+          const uint32_t vslot = v_n % C::kVSlots, vpar = (v_n / C::kVSlots) & 1;  // V_j, used at step j + 1
+          ++v_n;
+          ok = mbar_wait(bars.k_full(kslot), kpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          if (ok && j > 0) ok = mbar_wait(bars.v_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -289,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bars.s_full(t));
           }
           if (!ok) break;
-          mma_commit(kv_empty(kslot));
-          if (j > 0) mma_commit(kv_empty(prev_vslot));
+          mma_commit(bars.k_empty(kslot));
+          if (j > 0) mma_commit(bars.v_empty(prev_vslot));
           if (j == nt - 1) {
             mma_commit(bars.q_empty(0));
             if (ntq > 1) mma_commit(bars.q_empty(1));
@@ -299,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           prev_vpar = vpar;
         }
         if (!ok) break;
-        ok = mbar_wait(bars.kv_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        ok = mbar_wait(bars.v_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -314,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(bars.o_full(t));
         }
         if (!ok) break;
-        mma_commit(kv_empty(prev_vslot));
+        mma_commit(bars.v_empty(prev_vslot));
       }
       // Every MMA and every completion arrive must have landed before the CTA tears down.
       mma_commit(bars.drain());
@@ -350,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t sr[128];
         tmem_ld_x128(tS, sr);
-        float* s = reinterpret_cast<float*>(sr);
+        float(&s)[128] = *reinterpret_cast<float(*)[128]>(sr);
         if (valid < kTileRows) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -380,24 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = m_cand;
           }
         }
-        const float neg_m = -m;
-        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 4 independent pairs: short add chains
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {  // P(bf16) for 32 key columns -> 16 TMEM columns over S
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            float x0, x1;
-            fma2(x0, x1, s[32 * q4 + 2 * c], s[32 * q4 + 2 * c + 1], prm.c_scale, prm.c_scale, neg_m, neg_m);
-            const float p0 = ex2(x0);
-            const float p1 = ex2(x1);
-            add2(sum[2 * (c & 3)], sum[2 * (c & 3) + 1], sum[2 * (c & 3)], sum[2 * (c & 3) + 1], p0, p1);
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
-            pk[c] = *reinterpret_cast<uint32_t*>(&v2);
-          }
-          tmem_st_x16(tS + 16 * q4, pk);
-        }
-        l = l * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+        // P = 2^(s*c - m) in bf16 over S, and its row sum.
+        const float row_sum = exp_store_row(s, prm.c_scale, -m, tS);
+        l = l * alpha + row_sum;
         if (rescale) {  // warp-uniform: tcgen05.ld/st are warp-collective
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
