@@ -37,6 +37,8 @@ def parse():
     ap.add_argument("--workload", default="h3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--sweep", action="store_true",
+                    help="auxiliary: one JSON line per sweep point (kept TFLOP/s vs window density), 1 GPU")
     return ap.parse_args()
 
 
@@ -207,8 +209,60 @@ def run_reference(args, w, rank):
     }), flush=True)
 
 
+def max_over_ranks(x, device, world):
+    """The slowest rank's value (the job finishes when the last replica does)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, flops_per_replica, seconds):
+    """Whole-job TFLOP/s: every replica does the same kept-pair work; the job takes the slowest rank's time."""
+    return world * flops_per_replica / seconds / 1e12
+
+
+def run_sweep(args):
+    """Kept-pair throughput across the H3-shaped sweep (T in {34, 102}, K in {1, 3, 6}, r in {0, 1, 2})."""
+    import torch
+    import chunk_windowed_softmax_gb300 as wa
+    from chunk_windowed_softmax_gb300 import _build, configs, inputs
+    _build.build()
+    bf16_peak = peaks()[0]
+    for w in configs.sweep():
+        q, k, v = inputs.make_qkv(w, device="cuda")
+        plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+        info = plan.info()
+        out = torch.empty_like(q)
+        for _ in range(max(3, args.warmup)):
+            plan.forward(q, k, v, out=out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(3, min(args.steps, 10))
+        e0.record()
+        for _ in range(n):
+            plan.forward(q, k, v, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        st = plan.check_error()
+        plan.close()
+        ms = e0.elapsed_time(e1) / n
+        flops = 4.0 * w.D * info["kept_pairs"] * w.B * w.H
+        print(json.dumps({"workload": w.name, "T": w.T, "K": w.K, "r": w.r, "density": info["kept_pairs"] / w.L ** 2,
+                          "kept_tflop": flops / 1e12, "ms_per_call": ms, "tflops": flops / ms / 1e9,
+                          "pct_of_bf16_peak": 100 * flops / ms / 1e9 / bf16_peak, "status": wa.wa_status_string(st)}),
+              flush=True)
+        del q, k, v, out
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -269,12 +323,8 @@ def main():
     st = plan.check_error()
     if st != 0:
         raise SystemExit(f"device error during the timed steps: {wa.wa_status_string(st)}")
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = world * flops / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, dev, world)
+    value = job_throughput(world, flops, ms_max * 1e-3)
     attn_avg = attn_ms / max(1, nrec)
     bf16_peak, bf16_sus, hbm, peak_kind = peaks()
     achieved = flops / (attn_avg * 1e-3) / 1e12
@@ -291,12 +341,8 @@ def main():
     for _ in range(args.e2e_steps):
         wa.forward(qh, kh, vh, w.T, w.S, w.K, w.r, w.G, w.global_pos, out=oh)
     torch.cuda.synchronize(dev)
-    e2e_s = (time.perf_counter() - tt0) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * flops / e2e_s / 1e12
+    e2e_s = max_over_ranks((time.perf_counter() - tt0) / args.e2e_steps, dev, world)
+    e2e_value = job_throughput(world, flops, e2e_s)
     nbytes = q.numel() * q.element_size()
 
     cpu = None
