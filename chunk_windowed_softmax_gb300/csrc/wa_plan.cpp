@@ -18,6 +18,7 @@
 
 struct wa_plan {
   wa::HostPlan hp;
+  std::mutex mu;  // guards the per-call host state below (last stream, profiling records, debug flags)
   int device = -1;
   int num_sms = 0;
   int refcount = 0;
@@ -346,6 +347,7 @@ wa_status wa_plan_info(const wa_plan_t* plan, wa_plan_info_t* info) {
 // Test hook (not in the public header): set fault-injection flags of a plan.
 int wa_plan_set_debug_flags(wa_plan_t* plan, int flags) {
   if (!plan) return WA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(plan->mu);
   plan->debug_flags = flags;
   return WA_OK;
 }
@@ -374,6 +376,7 @@ wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* 
     return WA_ERR_INVALID;
   }
   cudaStream_t s = (cudaStream_t)stream;
+  std::lock_guard<std::mutex> lk(plan->mu);  // forwards on one plan share its workspace: serialise the host side
   if (plan->have_last && plan->last_stream != s) {
     if (cudaStreamWaitEvent(s, plan->done, 0) != cudaSuccess) return WA_ERR_CUDA;
   }
@@ -409,6 +412,7 @@ wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* 
 
 int wa_plan_profile(wa_plan_t* plan, int enable) {
   if (!plan) return WA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(plan->mu);
   plan->profiling = enable != 0;
   plan->prof_n = 0;
   return WA_OK;
@@ -416,6 +420,7 @@ int wa_plan_profile(wa_plan_t* plan, int enable) {
 
 int wa_plan_profile_read(wa_plan_t* plan, double* attention_ms, double* combine_ms, int* n_forwards) {
   if (!plan || !attention_ms || !combine_ms || !n_forwards) return WA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(plan->mu);
   *attention_ms = *combine_ms = 0.0;
   *n_forwards = plan->prof_n;
   for (int i = 0; i < plan->prof_n; ++i) {
