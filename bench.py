@@ -37,6 +37,8 @@ def parse():
     ap.add_argument("--workload", default="h3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--fp8", action="store_true",
+                    help="time wa_forward_fp8 (e4m3 queries / keys, per-tensor scales; bf16 values and output)")
     ap.add_argument("--sweep", action="store_true",
                     help="auxiliary: one JSON line per sweep point (kept TFLOP/s vs window density), 1 GPU")
     return ap.parse_args()
@@ -286,14 +288,24 @@ def main():
             dist.barrier()
 
     q, k, v = inputs.make_qkv(w, device=dev)
+    if args.fp8:
+        sq = float(q.float().abs().max()) / 448.0
+        sk = float(k.float().abs().max()) / 448.0
+        q8 = (q.float() / sq).to(torch.float8_e4m3fn)
+        k8 = (k.float() / sk).to(torch.float8_e4m3fn)
     plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+
+    def forward(out):
+        if args.fp8:
+            return plan.forward_fp8(q8, k8, v, sq, sk, out=out)
+        return plan.forward(q, k, v, out=out)
     info = plan.info()
     flops = 4.0 * w.D * info["kept_pairs"] * w.B * w.H
     launches_per_step = 1 + (1 if w.G > 0 else 0)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
-        plan.forward(q, k, v, out=out)
+        forward(out)
     st = plan.check_error()
     if st != 0:
         raise SystemExit(f"device error during warm-up: {wa.wa_status_string(st)}")
@@ -311,7 +323,7 @@ def main():
     t0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
-        plan.forward(q, k, v, out=out)
+        forward(out)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -329,6 +341,18 @@ def main():
     bf16_peak, bf16_sus, hbm, peak_kind = peaks()
     achieved = flops / (attn_avg * 1e-3) / 1e12
 
+    if args.fp8:  # the e4m3 path has no one-shot host-tensor call; report the device-resident line only
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": job_throughput(world, flops, ms_max * 1e-3),
+                              "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+                              "vs_baseline": None, "dtype": "e4m3 scores, bf16 P.V", "data": "synthetic",
+                              "config": workload_config(w), "kernel_ms": attn_ms / max(1, nrec),
+                              "merge_kernel_ms": comb_ms / max(1, nrec), "clocks": clocks}), flush=True)
+        plan.close()
+        if world > 1:
+            dist.destroy_process_group()
+        return
     # End to end through the public call with host tensors: pinned host -> device copies, the forward, and the
     # device -> host copy of the result, every step.
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))

@@ -18,7 +18,7 @@ STATUS = {0: "WA_OK", 1: "WA_ERR_INVALID", 2: "WA_ERR_UNSUPPORTED", 3: "WA_ERR_O
 # Symbols declared in include/wa.h (the tests check that the library exports each of them).
 EXPORTS = ("wa_plan_create", "wa_forward", "wa_plan_check_error", "wa_plan_info", "wa_plan_release",
            "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount",
-           "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static")
+           "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static", "wa_forward_fp8")
 
 
 class WAError(RuntimeError):
@@ -62,6 +62,8 @@ def lib():
         L.wa_plan_create.restype = ctypes.c_int
         L.wa_forward.argtypes = [P, P, P, P, P, P]
         L.wa_forward.restype = ctypes.c_int
+        L.wa_forward_fp8.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P]
+        L.wa_forward_fp8.restype = ctypes.c_int
         L.wa_plan_check_error.argtypes = [P, P]
         L.wa_plan_check_error.restype = ctypes.c_int
         L.wa_plan_info.argtypes = [P, ctypes.POINTER(wa_plan_info_t)]
@@ -119,6 +121,12 @@ def wa_plan_create(T, S, K, r, G, layout):
 def wa_forward(plan, q_ptr, k_ptr, v_ptr, out_ptr, stream_ptr):
     _check(lib().wa_forward(plan, ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                             ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream_ptr)), "wa_forward")
+
+
+def wa_forward_fp8(plan, q8_ptr, k8_ptr, v_ptr, out_ptr, q_scale, k_scale, stream_ptr):
+    _check(lib().wa_forward_fp8(plan, ctypes.c_void_p(q8_ptr), ctypes.c_void_p(k8_ptr), ctypes.c_void_p(v_ptr),
+                                ctypes.c_void_p(out_ptr), q_scale, k_scale, ctypes.c_void_p(stream_ptr)),
+           "wa_forward_fp8")
 
 
 def wa_forward_static(T, S, K, r, G, layout, q_ptr, k_ptr, v_ptr, out_ptr, stream_ptr):
@@ -188,6 +196,22 @@ class Plan:
                                       device=q.device)
         s = torch.cuda.current_stream(q.device) if stream is None else stream
         wa_forward(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), s.cuda_stream)
+        return out
+
+    def forward_fp8(self, q8, k8, v, q_scale, k_scale, out=None, stream=None):
+        """out <- window attention with e4m3 queries / keys (values q_scale * q8, k_scale * k8) and bf16 v."""
+        import torch
+        lay = self.layout
+        shape = (lay.B, self.L, lay.H, lay.D)
+        strides = (lay.stride_b, lay.stride_l, lay.stride_h, 1)
+        for name, t, dt in (("q8", q8, torch.float8_e4m3fn), ("k8", k8, torch.float8_e4m3fn), ("v", v, torch.bfloat16)):
+            if t.dtype != dt or not t.is_cuda or tuple(t.shape) != shape or tuple(t.stride()) != strides:
+                raise ValueError(f"{name} must be a {dt} CUDA tensor of shape {shape} with the plan's strides")
+        if out is None:
+            out = torch.empty_strided(shape, strides, dtype=torch.bfloat16, device=v.device)
+        s = torch.cuda.current_stream(v.device) if stream is None else stream
+        wa_forward_fp8(self.handle, q8.data_ptr(), k8.data_ptr(), v.data_ptr(), out.data_ptr(), float(q_scale),
+                       float(k_scale), s.cuda_stream)
         return out
 
     def check_error(self, stream=None):

@@ -49,26 +49,35 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O only 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms: waiting for in-flight copies while unwinding
 
-template <int D>
+// kF8: q and k are e4m3 (one byte per element) and the scores use kind::f8f6f4 MMAs; v, P and O stay bf16 / fp32.
+template <int D, bool kF8>
 struct Cfg {
-  static constexpr int kHalves = D / 64;              // 128-byte swizzle boxes per row
-  static constexpr int kHalfBytes = kTileRows * 128;  // one box: 128 rows x 64 bf16
-  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kQKRowBytes = D * (kF8 ? 1 : 2);
+  static constexpr int kQKBoxes = kQKRowBytes / 128;           // 128-byte swizzle boxes per q / k row
+  static constexpr int kQKBoxElems = kF8 ? 128 : 64;           // elements in one 128-byte box row
+  static constexpr int kQTileBytes = kTileRows * kQKRowBytes;  // one query tile (also one key tile)
+  static constexpr int kVBoxes = D / 64;                       // v is bf16: 64 elements per 128-byte box row
+  static constexpr int kVTileBytes = kTileRows * D * 2;
+  static constexpr int kBoxBytes = kTileRows * 128;            // one box: 128 rows x 128 bytes
+  static constexpr int kSKSteps = kF8 ? D / 32 : D / 16;       // score MMAs per tile (32 bytes of K each)
+  static_assert(kQKBoxes >= 1 && kQKRowBytes % 128 == 0, "q / k rows must be whole 128-byte boxes");
   // Separate K and V rings; the producer runs K one tile ahead of V (K is needed a step earlier than V).
-  static constexpr int kKSlots = D == 128 ? 3 : 4;
-  static constexpr int kVSlots = D == 128 ? 2 : 4;
+  static constexpr int kKSlots = kF8 ? 5 : (D == 128 ? 3 : 4);
+  static constexpr int kVSlots = kF8 ? 3 : (D == 128 ? 2 : 4);
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kKSlots * kTileBytes;
-  static constexpr int kBarOff = kVOff + kVSlots * kTileBytes;
+  static constexpr int kKOff = 2 * kQTileBytes;
+  static constexpr int kVOff = kKOff + kKSlots * kQTileBytes;
+  static constexpr int kBarOff = kVOff + kVSlots * kVTileBytes;
   // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain k_full[kKSlots] k_empty[kKSlots]
   //           v_full[kVSlots] v_empty[kVSlots]
   static constexpr int kNumBars = 11 + 2 * kKSlots + 2 * kVSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t kTmemO = 256;
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
+  static constexpr uint32_t kIdescS = kF8 ? idesc_e4m3_f32(128, 128)
+                                         : idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);   // P from TMEM, V MN-major (D contiguous)
+  static_assert(kBarOff + (11 + 2 * kKSlots + 2 * kVSlots) * 8 + 16 + 1024 <= 232448, "shared memory budget");
 };
 
 struct Params {
@@ -131,11 +140,11 @@ __device__ __forceinline__ float exp_store_row(const float (&s)[128], float c_sc
   return ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
 }
 
-template <int D>
+template <int D, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     window_attention_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const Params prm) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kF8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
@@ -218,11 +227,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((prm.debug_flags & 1) && !dropped && blockIdx.x == 0) {
           dropped = true;  // fault injection for the watchdog test: this tile is never loaded
         } else {
-          mbar_arrive_expect_tx(full, C::kTileBytes);
-          const uint32_t dst = (is_v ? sV : sK) + slot * C::kTileBytes;
+          if (is_v) {
+            mbar_arrive_expect_tx(full, C::kVTileBytes);
 #pragma unroll
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_4d(dst + hf * C::kHalfBytes, is_v ? &tmap_v : &tmap_k, full, hf * 64, h, row, b);
+            for (int hf = 0; hf < C::kVBoxes; ++hf)
+              tma_load_4d(sV + slot * C::kVTileBytes + hf * C::kBoxBytes, &tmap_v, full, hf * 64, h, row, b);
+          } else {
+            mbar_arrive_expect_tx(full, C::kQTileBytes);
+#pragma unroll
+            for (int hf = 0; hf < C::kQKBoxes; ++hf)
+              tma_load_4d(sK + slot * C::kQTileBytes + hf * C::kBoxBytes, &tmap_k, full, hf * C::kQKBoxElems, h,
+                          row, b);
+          }
         }
         n++;
         return true;
@@ -237,11 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t& qn = t ? q_n1 : q_n0;
           ok = mbar_wait(bars.q_empty(t), (qn & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           if (!ok) break;
-          mbar_arrive_expect_tx(bars.q_full(t), C::kTileBytes);
+          mbar_arrive_expect_tx(bars.q_full(t), C::kQTileBytes);
 #pragma unroll
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_4d(sQ + t * C::kTileBytes + hf * C::kHalfBytes, &tmap_q, bars.q_full(t), hf * 64, h,
-                        it.q_lo + t * kTileRows, b);
+          for (int hf = 0; hf < C::kQKBoxes; ++hf)
+            tma_load_4d(sQ + t * C::kQTileBytes + hf * C::kBoxBytes, &tmap_q, bars.q_full(t), hf * C::kQKBoxElems,
+                        h, it.q_lo + t * kTileRows, b);
           qn++;
         }
         const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
@@ -273,23 +289,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 14 bits: every address of the 227 KB window fits, so the addition never carries out of the field).
       const uint64_t dq = sdesc_sw128(sQ, 16, 1024);                 // Q tiles, K-major
       const uint64_t dk = sdesc_sw128(sK, 16, 1024);                 // K tiles, K-major
-      const uint64_t dv = sdesc_sw128(sV, C::kHalfBytes, 1024);      // V tiles, MN-major (D contiguous)
+      const uint64_t dv = sdesc_sw128(sV, C::kBoxBytes, 1024);       // V tiles, MN-major (D contiguous)
       // O_t (+)= P_t V, P_t read from TMEM (aliasing S_t), V from ring slot `vslot`
       auto issue_pv = [&](int t, uint32_t vslot, bool acc_first) {
-        const uint64_t d0 = dv + ((vslot * C::kTileBytes) >> 4);
+        const uint64_t d0 = dv + ((vslot * C::kVTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
           mma_ts(tmem + C::kTmemO + t * 128, tmem + t * 128 + kk * 8, d0 + ((kk * 2048) >> 4), C::kIdescPV,
                  (acc_first || kk > 0) ? 1u : 0u);
       };
-      // S_t = Q_t K^T, both K-major; K = D advances 32 bytes inside a 128-byte swizzle row, then to the next box
+      // S_t = Q_t K^T, both K-major; each MMA takes 32 bytes of K (16 bf16 or 32 e4m3 elements) inside a
+      // 128-byte swizzle row, then moves to the next box
       auto issue_s = [&](int t, uint32_t kslot) {
-        const uint64_t q0 = dq + ((t * C::kTileBytes) >> 4);
-        const uint64_t k0 = dk + ((kslot * C::kTileBytes) >> 4);
+        const uint64_t q0 = dq + ((t * C::kQTileBytes) >> 4);
+        const uint64_t k0 = dk + ((kslot * C::kQTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk / 4) * C::kHalfBytes + (kk % 4) * 32) >> 4;
-          mma_ss(tmem + t * 128, q0 + off, k0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < C::kSKSteps; ++kk) {
+          const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
+          if constexpr (kF8)
+            mma_ss_f8(tmem + t * 128, q0 + off, k0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + t * 128, q0 + off, k0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
@@ -538,32 +558,37 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map over (D, H, L, B) with a 64 x 1 x 128 x 1 box and 128-byte swizzle; rows past L read as zeros.
-bool make_map(CUtensorMap* m, const void* ptr, const Geometry& g) {
+// 4-D map over (D, H, L, B) with a (128 bytes) x 1 x 128 x 1 box and 128-byte swizzle; rows past L read as
+// zeros. elem_bytes 2: bf16; 1: e4m3 (as 8-bit integers: the copy does not interpret them).
+bool make_map(CUtensorMap* m, const void* ptr, const Geometry& g, int elem_bytes) {
   auto enc = encode_fn();
   if (!enc) return false;
   const wa_layout_t& l = g.layout;
+  const cuuint64_t eb = (cuuint64_t)elem_bytes;
   cuuint64_t dims[4] = {(cuuint64_t)l.D, (cuuint64_t)l.H, (cuuint64_t)g.L, (cuuint64_t)l.B};
-  cuuint64_t strides[3] = {(cuuint64_t)l.stride_h * 2, (cuuint64_t)l.stride_l * 2, (cuuint64_t)l.stride_b * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileRows, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)l.stride_h * eb, (cuuint64_t)l.stride_l * eb, (cuuint64_t)l.stride_b * eb};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / elem_bytes), 1, (cuuint32_t)kTileRows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+  return enc(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+             const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kF8>
 int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kF8>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<D, kF8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, *a.geo) || !make_map(&mk, a.k, *a.geo) || !make_map(&mv, a.v, *a.geo))
+  const int qk_bytes = kF8 ? 1 : 2;
+  if (!make_map(&mq, a.q, *a.geo, qk_bytes) || !make_map(&mk, a.k, *a.geo, qk_bytes) ||
+      !make_map(&mv, a.v, *a.geo, 2))
     return (int)cudaErrorInvalidValue;
   const wa_layout_t& l = a.geo->layout;
   Params p;
@@ -580,10 +605,10 @@ int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
   p.G = a.geo->G;
   p.g0 = (int)a.geo->g0;
   p.n_splits = a.n_splits;
-  p.c_scale = (float)(1.4426950408889634 / sqrt((double)D));
+  p.c_scale = (float)(1.4426950408889634 / sqrt((double)D) * (double)a.qk_scale);
   p.debug_flags = a.debug_flags;
   const int grid = a.n_items < num_sms ? a.n_items : num_sms;
-  window_attention_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
+  window_attention_kernel<D, kF8><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
   return (int)cudaGetLastError();
 }
 
@@ -591,7 +616,9 @@ int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
 
 int launch_attention(const LaunchArgs& a, void* stream, int num_sms) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return a.geo->layout.D == 128 ? launch_attention_d<128>(a, s, num_sms) : launch_attention_d<64>(a, s, num_sms);
+  if (a.qk_fp8) return a.geo->layout.D == 128 ? launch_attention_d<128, true>(a, s, num_sms) : (int)cudaErrorInvalidValue;
+  return a.geo->layout.D == 128 ? launch_attention_d<128, false>(a, s, num_sms)
+                                : launch_attention_d<64, false>(a, s, num_sms);
 }
 
 int launch_combine(const LaunchArgs& a, void* stream) {

@@ -11,6 +11,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <list>
 #include <mutex>
 
@@ -359,15 +360,23 @@ int wa_cache_size(void) {
 }
 int wa_plan_refcount(const wa_plan_t* plan) { return plan ? plan->refcount : -1; }
 
-wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the forward entry points. qk_bytes: element size of q and k (2 bf16, 1 e4m3); qk_scale multiplies
+// the scores (the product of the e4m3 tensors' dequantisation factors; 1 for bf16).
+wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream,
+                       int qk_bytes, float qk_scale) {
   if (!plan || !q || !k || !v || !out) return WA_ERR_INVALID;
   auto al = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
   if (!al(q) || !al(k) || !al(v) || !al(out)) return WA_ERR_INVALID;
   const wa::Geometry& g = plan->hp.geo;
   const wa_layout_t& l = g.layout;
-  const size_t span = 2 * (size_t)((l.B - 1) * l.stride_b + (g.L - 1) * l.stride_l + (l.H - 1) * l.stride_h + l.D);
+  const size_t elems = (size_t)((l.B - 1) * l.stride_b + (g.L - 1) * l.stride_l + (l.H - 1) * l.stride_h + l.D);
+  const size_t span = 2 * elems, qk_span = (size_t)qk_bytes * elems;
   uintptr_t o = (uintptr_t)out;
-  if (ranges_overlap(o, span, (uintptr_t)q, span) || ranges_overlap(o, span, (uintptr_t)k, span) ||
+  if (ranges_overlap(o, span, (uintptr_t)q, qk_span) || ranges_overlap(o, span, (uintptr_t)k, qk_span) ||
       ranges_overlap(o, span, (uintptr_t)v, span))
     return WA_ERR_INVALID;
   int dev = -1;
@@ -390,6 +399,8 @@ wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* 
   a.n_splits = plan->hp.n_splits;
   a.debug_flags = plan->debug_flags;
   a.geo = &g;
+  a.qk_fp8 = qk_bytes == 1;
+  a.qk_scale = qk_scale;
   cudaEvent_t* ev = nullptr;
   if (plan->profiling && plan->prof_n < kMaxProfiled) {
     while ((int)plan->prof_ev.size() < 3 * (plan->prof_n + 1)) {
@@ -408,6 +419,24 @@ wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* 
   plan->last_stream = s;
   plan->have_last = true;
   return WA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream) {
+  return forward_impl(plan, q, k, v, out, stream, 2, 1.0f);
+}
+
+wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const void* v, void* out, float q_scale,
+                         float k_scale, wa_stream_t stream) {
+  if (!plan) return WA_ERR_INVALID;
+  if (!(q_scale > 0.f) || !(k_scale > 0.f) || !std::isfinite(q_scale) || !std::isfinite(k_scale) ||
+      !std::isfinite(q_scale * k_scale))
+    return WA_ERR_INVALID;
+  if (plan->hp.geo.layout.D != 128) return WA_ERR_UNSUPPORTED;
+  return forward_impl(plan, q8, k8, v, out, stream, 1, q_scale * k_scale);
 }
 
 int wa_plan_profile(wa_plan_t* plan, int enable) {

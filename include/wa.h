@@ -103,6 +103,20 @@ wa_status wa_plan_create(int T, int S, int K, int r, int G, const wa_layout_t* l
 wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream);
 
 /*
+ * out <- window attention with 8-bit queries and keys (the article's deployment runs the model in FP8,
+ * section 四: 6.41 s/NFE FP8 on one GPU; this is the attention-side counterpart).
+ *   q8, k8: device pointers to e4m3 (float8 e4m3fn, 1 byte) [B, L, H, D] with the plan's element strides; the
+ *           represented values are q = q_scale * q8 and k = k_scale * k8 (per-tensor dequantisation factors).
+ *   v, out: bf16 as in wa_forward.
+ * Scores are q8.k8 (exact products, fp32 accumulation by kind::f8f6f4 MMAs) times q_scale * k_scale / sqrt(D);
+ * the softmax, P (bf16) and O (fp32 accumulation) are as in wa_forward. Uses the same plan as wa_forward.
+ * Errors: as wa_forward; WA_ERR_INVALID for scales that are not finite and positive; WA_ERR_UNSUPPORTED unless
+ * D == 128 (one e4m3 row is then exactly one 128-byte swizzle row).
+ */
+wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const void* v, void* out, float q_scale,
+                         float k_scale, wa_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the plan's device error word.
  * Returns WA_OK, WA_ERR_DEVICE_TIMEOUT, WA_ERR_DEVICE_BOUNDS, or WA_ERR_CUDA if the synchronisation failed.
  */
