@@ -286,30 +286,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_n0 = 0, q_n1 = 0, p_n0 = 0, p_n1 = 0;
       bool ok = true;
       // Descriptors are built once; a shared-memory offset is added to the start-address field (address >> 4,
-      // 14 bits: every address of the 227 KB window fits, so the addition never carries out of the field).
+      // 14 bits: every address of the 227 KB window fits, so the addition never carries out of the field, nor out
+      // of the low word).
       const uint64_t dq = sdesc_sw128(sQ, 16, 1024);                 // Q tiles, K-major
       const uint64_t dk = sdesc_sw128(sK, 16, 1024);                 // K tiles, K-major
       const uint64_t dv = sdesc_sw128(sV, C::kBoxBytes, 1024);       // V tiles, MN-major (D contiguous)
       // O_t (+)= P_t V, P_t read from TMEM (aliasing S_t), V from ring slot `vslot`
+      // All three descriptor families share one high word (stride byte offset 1024, version, 128-byte swizzle).
+      const uint32_t desc_hi = (uint32_t)(dq >> 32);
       auto issue_pv = [&](int t, uint32_t vslot, bool acc_first) {
-        const uint64_t d0 = dv + ((vslot * C::kVTileBytes) >> 4);
+        const uint32_t d0 = (uint32_t)dv + ((vslot * C::kVTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_ts(tmem + C::kTmemO + t * 128, tmem + t * 128 + kk * 8, d0 + ((kk * 2048) >> 4), C::kIdescPV,
-                 (acc_first || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kTmemO + t * 128, tmem + t * 128 + kk * 8, d0 + ((kk * 2048) >> 4), desc_hi,
+                 C::kIdescPV, (acc_first || kk > 0) ? 1u : 0u);
       };
       // S_t = Q_t K^T, both K-major; each MMA takes 32 bytes of K (16 bf16 or 32 e4m3 elements) inside a
       // 128-byte swizzle row, then moves to the next box
       auto issue_s = [&](int t, uint32_t kslot) {
-        const uint64_t q0 = dq + ((t * C::kQTileBytes) >> 4);
-        const uint64_t k0 = dk + ((kslot * C::kQTileBytes) >> 4);
+        const uint32_t q0 = (uint32_t)dq + ((t * C::kQTileBytes) >> 4);
+        const uint32_t k0 = (uint32_t)dk + ((kslot * C::kQTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::kSKSteps; ++kk) {
           const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
           if constexpr (kF8)
-            mma_ss_f8(tmem + t * 128, q0 + off, k0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss_f8(tmem + t * 128, q0 + off, k0 + off, desc_hi, C::kIdescS, kk > 0 ? 1u : 0u);
           else
-            mma_ss(tmem + t * 128, q0 + off, k0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + t * 128, q0 + off, k0 + off, desc_hi, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {

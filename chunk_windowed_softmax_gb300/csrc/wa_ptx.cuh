@@ -113,42 +113,54 @@ __device__ __forceinline__ void regs_dec() {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+// The shared-memory descriptors of one operand family differ only in their low 32 bits (start address and leading
+// byte offset); the MMA wrappers take those low words plus the common high word, so that advancing through a tile
+// costs one 32-bit add per operand and MMA (the issuing thread shares its sub-partition with busy warps).
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs (kind::f16; K = 16 per instruction)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
       "{\n"
       "  .reg .pred p;\n"
-      "  setp.ne.b32 p, %4, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "  .reg .b64 da, db;\n"
+      "  mov.b64 da, {%1, %3};\n"
+      "  mov.b64 db, {%2, %3};\n"
+      "  setp.ne.b32 p, %5, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n"
       "}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem], 8-bit floating-point inputs (kind::f8f6f4; K = 32 per instruction)
-__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
       "{\n"
       "  .reg .pred p;\n"
-      "  setp.ne.b32 p, %4, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+      "  .reg .b64 da, db;\n"
+      "  mov.b64 da, {%1, %3};\n"
+      "  mov.b64 db, {%2, %3};\n"
+      "  setp.ne.b32 p, %5, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n"
       "}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+// D[tmem] (+)= A[tmem] * B[smem], bf16 inputs
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
       "{\n"
       "  .reg .pred p;\n"
-      "  setp.ne.b32 p, %4, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "  .reg .b64 db;\n"
+      "  mov.b64 db, {%2, %3};\n"
+      "  setp.ne.b32 p, %5, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n"
       "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
