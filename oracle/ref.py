@@ -18,6 +18,10 @@ Readings where the article is silent (each one is listed with its reason in the 
   * globals sit after the frame tokens (global_pos = 0) or before them (global_pos = 1);
   * scores are scaled by 1/sqrt(D); non-causal; no bias, softcap or dropout.
 
+The backward (window_attention_backward, row_logsumexp) follows the same loop and is pinned by
+tests/test_oracle_backward.py: central finite differences of the forward above, and torch autograd through a
+float64 dense attention in the cases that reduce to one.
+
 Every function here is pinned by tests/test_oracle.py against facts that do not come from this file
 (brute force over an explicit mask, a library dense-attention routine in the special cases that reduce to it,
 closed forms and invariants), so no function is "parity unpinned".
@@ -168,3 +172,58 @@ def kept_pairs(T, S, K, r, G, global_pos=0):
     for t in range(T):
         n += S * len(kept_set_of_frame(t, T, S, K, r, G, global_pos))
     return n + G * (T * S + G)
+
+
+# ------------------------------------------------------------------------------------------------ backward
+def row_logsumexp(q, k, T, S, K, r, G, global_pos):
+    """LSE_i = ln sum_{j in kept(i)} exp(q_i.k_j / sqrt(D)) for every row, float64 [B, H, L]."""
+    q, k = _as64(q), _as64(k)
+    B, L, H, D = q.shape
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros((B, H, L))
+    f0, g0 = frame_offset(G, global_pos), global_offset(T, S, global_pos)
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                kept = kept_set_of_frame(t, T, S, K, r, G, global_pos)
+                rows = frame_rows(t, S, f0)
+                s = (q[b, rows, h] @ k[b, kept, h].T) * scale
+                mx = s.max(axis=1, keepdims=True)
+                out[b, h, rows] = (mx + np.log(np.exp(s - mx).sum(axis=1, keepdims=True)))[:, 0]
+            if G:
+                rows = np.arange(g0, g0 + G)
+                s = (q[b, rows, h] @ k[b, :, h].T) * scale
+                mx = s.max(axis=1, keepdims=True)
+                out[b, h, rows] = (mx + np.log(np.exp(s - mx).sum(axis=1, keepdims=True)))[:, 0]
+    return out
+
+
+def window_attention_backward(q, k, v, dout, T, S, K, r, G, global_pos):
+    """Gradients (dq, dk, dv) of sum(out * dout) for the chunk-window attention, float64, by the same per-frame loop.
+
+    For a row i with kept set J (scale c = 1/sqrt(D)): p = softmax_J(c q_i.k_j); o_i = sum p_j v_j. Then
+    dv_j += p_j dout_i; dp_j = dout_i.v_j; ds_j = p_j (dp_j - sum_j' p_j' dp_j'); dq_i = c sum_j ds_j k_j;
+    dk_j += c ds_j q_i (the chain rule through the softmax restricted to J).
+    """
+    q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
+    B, L, H, D = q.shape
+    scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    f0, g0 = frame_offset(G, global_pos), global_offset(T, S, global_pos)
+
+    def rows_backward(b, h, rows, kept):
+        _, p = attend(q[b, rows, h], k[b, kept, h], v[b, kept, h], scale)
+        do = dout[b, rows, h]
+        dv[b, kept, h] += p.T @ do
+        dp = do @ v[b, kept, h].T
+        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        dq[b, rows, h] += scale * (ds @ k[b, kept, h])
+        dk[b, kept, h] += scale * (ds.T @ q[b, rows, h])
+
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                rows_backward(b, h, frame_rows(t, S, f0), kept_set_of_frame(t, T, S, K, r, G, global_pos))
+            if G:
+                rows_backward(b, h, np.arange(g0, g0 + G), kept_set_of_global(T, S, G))
+    return dq, dk, dv
