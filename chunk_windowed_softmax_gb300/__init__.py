@@ -18,7 +18,7 @@ STATUS = {0: "WA_OK", 1: "WA_ERR_INVALID", 2: "WA_ERR_UNSUPPORTED", 3: "WA_ERR_O
 # Symbols declared in include/wa.h (the tests check that the library exports each of them).
 EXPORTS = ("wa_plan_create", "wa_forward", "wa_plan_check_error", "wa_plan_info", "wa_plan_release",
            "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount",
-           "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static", "wa_forward_fp8")
+           "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static", "wa_forward_fp8", "wa_forward_lse")
 
 
 class WAError(RuntimeError):
@@ -62,6 +62,8 @@ def lib():
         L.wa_plan_create.restype = ctypes.c_int
         L.wa_forward.argtypes = [P, P, P, P, P, P]
         L.wa_forward.restype = ctypes.c_int
+        L.wa_forward_lse.argtypes = [P, P, P, P, P, P, P]
+        L.wa_forward_lse.restype = ctypes.c_int
         L.wa_forward_fp8.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P]
         L.wa_forward_fp8.restype = ctypes.c_int
         L.wa_plan_check_error.argtypes = [P, P]
@@ -197,6 +199,25 @@ class Plan:
         s = torch.cuda.current_stream(q.device) if stream is None else stream
         wa_forward(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), s.cuda_stream)
         return out
+
+    def forward_lse(self, q, k, v, out=None, lse=None, stream=None):
+        """(out, lse): the forward and each row's natural-log log-sum-exp (fp32 [B, H, L]) for the backward."""
+        import torch
+        lay = self.layout
+        if lse is None:
+            lse = torch.empty(lay.B, lay.H, self.L, dtype=torch.float32, device=q.device)
+        shape = (lay.B, self.L, lay.H, lay.D)
+        strides = (lay.stride_b, lay.stride_l, lay.stride_h, 1)
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or tuple(t.shape) != shape or tuple(t.stride()) != strides:
+                raise ValueError(f"{name} must be a bf16 CUDA tensor of shape {shape} with the plan's strides")
+        if out is None:
+            out = torch.empty_strided(shape, strides, dtype=torch.bfloat16, device=q.device)
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        _check(lib().wa_forward_lse(self.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                                    ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                    ctypes.c_void_p(lse.data_ptr()), ctypes.c_void_p(s.cuda_stream)), "wa_forward_lse")
+        return out, lse
 
     def forward_fp8(self, q8, k8, v, q_scale, k_scale, out=None, stream=None):
         """out <- window attention with e4m3 queries / keys (values q_scale * q8, k_scale * k8) and bf16 v."""

@@ -57,6 +57,7 @@ struct LaunchArgs {
   int n_splits;
   int debug_flags;  // test-only fault injection on the host-visible error path (0 in normal use)
   const Geometry* geo;
+  float* lse = nullptr;    // optional [B][H][L] fp32 output: natural-log sum of exp of each row's scaled scores
   int qk_fp8 = 0;          // q and k are e4m3 (scores by kind::f8f6f4 MMAs); v and out stay bf16
   float qk_scale = 1.0f;   // dequantisation factor of the scores: q_scale * k_scale (1 for bf16 inputs)
 };

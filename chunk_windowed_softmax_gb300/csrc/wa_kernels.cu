@@ -91,6 +91,8 @@ struct Params {
   int H, G, g0, n_splits;
   float c_scale;  // log2(e) / sqrt(D)
   int debug_flags;
+  float* lse;     // optional [B][H][L] row log-sum-exp output (natural log); nullptr when not wanted
+  int L;
 };
 
 // Shared-memory barrier layout, relative to the barrier block: q_full[2] q_empty[2] s_full[2] p_full[2]
@@ -492,6 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 4; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
           }
         }
+        if (prm.lse != nullptr && row_ok)  // m and l are in log2 units of the scaled score
+          prm.lse[(int64_t)it.bh * prm.L + row] = (m + __log2f(l)) * 0.6931471805599453f;
       } else {
         const int64_t grow = (int64_t)row - prm.g0;
         const int64_t slot = ((int64_t)it.bh * prm.G + grow) * prm.n_splits + it.split;
@@ -521,7 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                                                       __nv_bfloat16* __restrict__ out, int rows, int G, int H, int g0,
-                                                      int P, int64_t sb, int64_t sl, int64_t sh) {
+                                                      int P, int64_t sb, int64_t sl, int64_t sh, float* lse_out,
+                                                      int L) {
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -546,6 +551,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   __nv_bfloat16* dst = out + (int64_t)b * sb + (int64_t)(g0 + gr) * sl + (int64_t)h * sh;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) dst[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+  if (lse_out != nullptr && lane == 0) lse_out[(int64_t)bh * L + g0 + gr] = (mx + __log2f(den)) * 0.6931471805599453f;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -610,6 +616,8 @@ int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
   p.n_splits = a.n_splits;
   p.c_scale = (float)(1.4426950408889634 / sqrt((double)D) * (double)a.qk_scale);
   p.debug_flags = a.debug_flags;
+  p.lse = a.lse;
+  p.L = (int)a.geo->L;
   const int grid = a.n_items < num_sms ? a.n_items : num_sms;
   window_attention_kernel<D, kF8><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
   return (int)cudaGetLastError();
@@ -632,10 +640,12 @@ int launch_combine(const LaunchArgs& a, void* stream) {
   const int blocks = (rows + 7) / 8;
   if (l.D == 128)
     combine_kernel<128><<<blocks, 256, 0, s>>>(a.ws_o, a.ws_lse, reinterpret_cast<__nv_bfloat16*>(a.out), rows, g.G,
-                                               l.H, (int)g.g0, a.n_splits, l.stride_b, l.stride_l, l.stride_h);
+                                               l.H, (int)g.g0, a.n_splits, l.stride_b, l.stride_l, l.stride_h, a.lse,
+                                               (int)g.L);
   else
     combine_kernel<64><<<blocks, 256, 0, s>>>(a.ws_o, a.ws_lse, reinterpret_cast<__nv_bfloat16*>(a.out), rows, g.G,
-                                              l.H, (int)g.g0, a.n_splits, l.stride_b, l.stride_l, l.stride_h);
+                                              l.H, (int)g.g0, a.n_splits, l.stride_b, l.stride_l, l.stride_h, a.lse,
+                                              (int)g.L);
   return (int)cudaGetLastError();
 }
 

@@ -367,8 +367,9 @@ namespace {
 // Shared body of the forward entry points. qk_bytes: element size of q and k (2 bf16, 1 e4m3); qk_scale multiplies
 // the scores (the product of the e4m3 tensors' dequantisation factors; 1 for bf16).
 wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream,
-                       int qk_bytes, float qk_scale) {
+                       int qk_bytes, float qk_scale, float* lse = nullptr) {
   if (!plan || !q || !k || !v || !out) return WA_ERR_INVALID;
+  if (lse && ((uintptr_t)lse & 3)) return WA_ERR_INVALID;
   auto al = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
   if (!al(q) || !al(k) || !al(v) || !al(out)) return WA_ERR_INVALID;
   const wa::Geometry& g = plan->hp.geo;
@@ -401,6 +402,7 @@ wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void
   a.geo = &g;
   a.qk_fp8 = qk_bytes == 1;
   a.qk_scale = qk_scale;
+  a.lse = lse;
   cudaEvent_t* ev = nullptr;
   if (plan->profiling && plan->prof_n < kMaxProfiled) {
     while ((int)plan->prof_ev.size() < 3 * (plan->prof_n + 1)) {
@@ -427,6 +429,12 @@ extern "C" {
 
 wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream) {
   return forward_impl(plan, q, k, v, out, stream, 2, 1.0f);
+}
+
+wa_status wa_forward_lse(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, float* lse,
+                         wa_stream_t stream) {
+  if (!lse) return WA_ERR_INVALID;
+  return forward_impl(plan, q, k, v, out, stream, 2, 1.0f, lse);
 }
 
 wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const void* v, void* out, float q_scale,

@@ -103,6 +103,15 @@ wa_status wa_plan_create(int T, int S, int K, int r, int G, const wa_layout_t* l
 wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream);
 
 /*
+ * wa_forward, and also the log-sum-exp of every row's scaled scores over its kept set, as the backward pass needs:
+ *   lse[(b*H + h)*L + i] = ln sum_{j kept by i} exp(q_i.k_j / sqrt(D))   (fp32, device, [B][H][L] contiguous,
+ *   4-byte aligned; every element is written).
+ * Errors: as wa_forward; WA_ERR_INVALID for a NULL or misaligned lse.
+ */
+wa_status wa_forward_lse(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, float* lse,
+                         wa_stream_t stream);
+
+/*
  * out <- window attention with 8-bit queries and keys (the article's deployment runs the model in FP8,
  * section 四: 6.41 s/NFE FP8 on one GPU; this is the attention-side counterpart).
  *   q8, k8: device pointers to e4m3 (float8 e4m3fn, 1 byte) [B, L, H, D] with the plan's element strides; the
