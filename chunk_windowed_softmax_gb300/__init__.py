@@ -18,7 +18,8 @@ STATUS = {0: "WA_OK", 1: "WA_ERR_INVALID", 2: "WA_ERR_UNSUPPORTED", 3: "WA_ERR_O
 # Symbols declared in include/wa.h (the tests check that the library exports each of them).
 EXPORTS = ("wa_plan_create", "wa_forward", "wa_plan_check_error", "wa_plan_info", "wa_plan_release",
            "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount",
-           "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static", "wa_forward_fp8", "wa_forward_lse")
+           "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static", "wa_forward_fp8", "wa_forward_lse",
+           "wa_backward", "wa_plan_profile_read_backward")
 
 
 class WAError(RuntimeError):
@@ -64,6 +65,10 @@ def lib():
         L.wa_forward.restype = ctypes.c_int
         L.wa_forward_lse.argtypes = [P, P, P, P, P, P, P]
         L.wa_forward_lse.restype = ctypes.c_int
+        L.wa_backward.argtypes = [P] * 11
+        L.wa_backward.restype = ctypes.c_int
+        L.wa_plan_profile_read_backward.argtypes = [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
+        L.wa_plan_profile_read_backward.restype = ctypes.c_int
         L.wa_forward_fp8.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P]
         L.wa_forward_fp8.restype = ctypes.c_int
         L.wa_plan_check_error.argtypes = [P, P]
@@ -123,6 +128,12 @@ def wa_plan_create(T, S, K, r, G, layout):
 def wa_forward(plan, q_ptr, k_ptr, v_ptr, out_ptr, stream_ptr):
     _check(lib().wa_forward(plan, ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                             ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream_ptr)), "wa_forward")
+
+
+def wa_backward(plan, q_ptr, k_ptr, v_ptr, out_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, stream_ptr):
+    _check(lib().wa_backward(plan, *(ctypes.c_void_p(p) for p in (q_ptr, k_ptr, v_ptr, out_ptr, dout_ptr, lse_ptr,
+                                                                  dq_ptr, dk_ptr, dv_ptr, stream_ptr))),
+           "wa_backward")
 
 
 def wa_forward_fp8(plan, q8_ptr, k8_ptr, v_ptr, out_ptr, q_scale, k_scale, stream_ptr):
@@ -218,6 +229,31 @@ class Plan:
                                     ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
                                     ctypes.c_void_p(lse.data_ptr()), ctypes.c_void_p(s.cuda_stream)), "wa_forward_lse")
         return out, lse
+
+    def backward(self, q, k, v, out, dout, lse, dq=None, dk=None, dv=None, stream=None):
+        """(dq, dk, dv): gradients through the forward, given dout and the forward's out and lse (forward_lse)."""
+        import torch
+        lay = self.layout
+        shape = (lay.B, self.L, lay.H, lay.D)
+        strides = (lay.stride_b, lay.stride_l, lay.stride_h, 1)
+        for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or tuple(t.shape) != shape or tuple(t.stride()) != strides:
+                raise ValueError(f"{name} must be a bf16 CUDA tensor of shape {shape} with the plan's strides")
+        if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (lay.B, lay.H, self.L) \
+                or not lse.is_contiguous():
+            raise ValueError(f"lse must be a contiguous fp32 CUDA tensor of shape {(lay.B, lay.H, self.L)}")
+        grads = [g if g is not None else torch.empty_strided(shape, strides, dtype=torch.bfloat16, device=q.device)
+                 for g in (dq, dk, dv)]
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        wa_backward(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                    lse.data_ptr(), *(g.data_ptr() for g in grads), s.cuda_stream)
+        return tuple(grads)
+
+    def profile_read_backward(self):
+        """([row dots, dq kernel, dk/dv kernel, split sums] ms, backwards) summed over the recorded backwards."""
+        ms, n = (ctypes.c_double * 4)(), ctypes.c_int()
+        _check(lib().wa_plan_profile_read_backward(self.handle, ms, ctypes.byref(n)), "wa_plan_profile_read_backward")
+        return list(ms), n.value
 
     def forward_fp8(self, q8, k8, v, q_scale, k_scale, out=None, stream=None):
         """out <- window attention with e4m3 queries / keys (values q_scale * q8, k_scale * k8) and bf16 v."""

@@ -9,7 +9,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwa.so")
-SOURCES = ["wa_plan.cpp", "wa_kernels.cu", "wa_noalloc.cu"]
+SOURCES = ["wa_plan.cpp", "wa_kernels.cu", "wa_backward.cu", "wa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,861 @@
+// Backward pass of chunk-aligned window softmax attention on sm_103a: dq, dk, dv of sum(out * dout).
+//
+// The kept relation is symmetric. A frame key of chunk c is kept by exactly the frame queries of the chunks
+// within r of c (the clamped window of c itself) and by every global query; a global key is kept by every query
+// (VDN-Minimax-H3 window-attention article, section 一: chunk window plus fully connected globals). So the
+// forward's work list serves the whole backward:
+//   * read query-major (item rows = queries, segments = their keys) it drives the dq kernel;
+//   * read key-major (item rows = keys, segments = the queries that keep them) it drives the dk / dv kernel.
+// Both kernels recompute the probabilities from the forward's row log-sum-exp, P = exp(s / sqrt(D) - lse), with the
+// scores s from tcgen05 MMAs, so no probability matrix is ever stored. Per (b, h), with c = 1 / sqrt(D):
+//   Dvec_i = dout_i . out_i,  dP_ij = dout_i . v_j,  dS_ij = P_ij (dP_ij - Dvec_i),
+//   dq_i = c sum_j dS_ij k_j,  dk_j = c sum_i dS_ij q_i,  dv_j = sum_i P_ij dout_i.
+// The global rows' dq (and the global keys' dk, dv) are split along the other operand like the forward's global
+// leg: each split writes an fp32 partial and bwd_sum_kernel adds the splits in a fixed order (deterministic).
+//
+// Every wait is bounded; on expiry a kernel latches an error in the plan's error word and unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "wa_internal.h"
+#include "wa_ptx.cuh"
+
+namespace wa {
+namespace {
+
+using namespace ptx;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms: waiting for in-flight copies while unwinding
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kBwdThreads = 192;  // warps 0-3 elementwise, warp 4 MMA issuer, warp 5 loads
+
+struct BwdParams {
+  const Item* items;
+  int n_items;
+  const float* lse;   // [B*H][L] natural-log row log-sum-exp of the forward
+  const float* dvec;  // [B*H][L] dout_i . out_i
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* ws_dq;       // [B*H][G][n_splits][D] fp32 partials of the global rows (dq) / global keys (dk, dv)
+  float* ws_dk;
+  float* ws_dv;
+  int* err;
+  int64_t sb, sl, sh;
+  int H, G, g0, L, n_splits;
+  float c_log2;       // log2(e) / sqrt(D): turns a raw score into log2 units of the scaled score
+  float scale;        // 1 / sqrt(D)
+  int debug_flags;
+};
+
+__device__ __forceinline__ Item load_item(const Item* items, int idx) {
+  const int4* p = reinterpret_cast<const int4*>(items + idx);
+  int4 a = __ldg(p), b = __ldg(p + 1);
+  return Item{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+}
+
+__device__ __forceinline__ int seg_tiles(int lo, int hi) { return hi > lo ? (hi - lo + kTileRows - 1) / kTileRows : 0; }
+
+// First row of the j-th 128-row tile of an item's segments, and how many of its rows belong to the segment.
+__device__ __forceinline__ int step_row(const Item& it, int j, int nt0, int* valid) {
+  const int lo = j < nt0 ? it.s0_lo + j * kTileRows : it.s1_lo + (j - nt0) * kTileRows;
+  const int hi = j < nt0 ? it.s0_hi : it.s1_hi;
+  *valid = min(kTileRows, hi - lo);
+  return lo;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v2 = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v2);
+}
+
+// One 128-row tile of a [B, L, H, D] bf16 tensor: D / 64 boxes of 128 rows x 128 bytes (128-byte swizzle).
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int h, int row, int b) {
+#pragma unroll
+  for (int hf = 0; hf < D / 64; ++hf) tma_load_4d(dst + hf * kTileRows * 128, map, bar, hf * 64, h, row, b);
+}
+
+// One accumulator row (fp32 in TMEM, D columns) times `mul`: bf16 into `dst`, or fp32 into `part` when that is set.
+template <int D>
+__device__ __forceinline__ void store_row(uint32_t t_acc, float mul, bool row_ok, __nv_bfloat16* dst, float* part) {
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t o[32];
+    tmem_ld_x32(t_acc + c0, o);  // warp-collective: every lane loads, only rows that exist store
+    if (!row_ok) continue;
+    if (part != nullptr) {
+      float4* d4 = reinterpret_cast<float4*>(part + c0);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        d4[c] = make_float4(__uint_as_float(o[4 * c]) * mul, __uint_as_float(o[4 * c + 1]) * mul,
+                            __uint_as_float(o[4 * c + 2]) * mul, __uint_as_float(o[4 * c + 3]) * mul);
+    } else {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        d4[c] = make_uint4(pack_bf16(__uint_as_float(o[8 * c]) * mul, __uint_as_float(o[8 * c + 1]) * mul),
+                           pack_bf16(__uint_as_float(o[8 * c + 2]) * mul, __uint_as_float(o[8 * c + 3]) * mul),
+                           pack_bf16(__uint_as_float(o[8 * c + 4]) * mul, __uint_as_float(o[8 * c + 5]) * mul),
+                           pack_bf16(__uint_as_float(o[8 * c + 6]) * mul, __uint_as_float(o[8 * c + 7]) * mul));
+    }
+  }
+}
+
+struct Smem {
+  uint8_t* p;
+  uint32_t base;
+};
+
+// The dynamic shared-memory window rounded up to 1024 bytes (the 128-byte swizzle repeats every 1024 bytes).
+__device__ __forceinline__ Smem align_smem(uint8_t* raw) {
+  uint8_t* s = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  return Smem{s, smem_u32(s)};
+}
+
+// Every thread: wait for all roles, then warp 0 frees the tensor memory.
+__device__ __forceinline__ void teardown(uint32_t tmem, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    __syncwarp();  // tcgen05.dealloc is warp-collective: reconverge after the role branches
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =====================================================================================================================
+// dq kernel: query-major. Each work item's query tiles are processed one after the other ("sub-items"), each against
+// the item's key segments, one 128-key tile per step.
+//   warps 0-3  elementwise: one thread per query row (TMEM lane); P = 2^(s c' - lse'), dS = P (dP - Dvec) as bf16
+//   warp 4     MMA issuer (one thread): S = Q K^T, dP = dout V^T, dq += dS K
+//   warp 5     TMA producer (one thread): Q and dout tiles of the sub-item, rings of key and value tiles
+// TMEM: R0, R1 [0,256) score buffers (step n's S in R[n % 2]; dS overwrites its first 64 columns as bf16 and is
+// the A operand of dS.K straight from TMEM), R2 [256,384) dP, R3 [384, 384+D) the dq accumulator. The next step's
+// S and dP are issued before this step's dS.K, so the elementwise work of a step overlaps the tensor core's.
+// =====================================================================================================================
+template <int D>
+struct DqCfg {
+  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kKSlots = 3, kVSlots = 2;
+  static constexpr int kQOff = 0, kDOOff = kTileBytes;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kKSlots * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVSlots * kTileBytes;
+  // q_full, q_empty, s_full[2], p_full[2], dp_free, o_full, drain, then the rings' full / empty barriers
+  static constexpr int kNumBars = 9 + 2 * kKSlots + 2 * kVSlots;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack of the dynamic window
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
+  static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);   // dS from TMEM, key tile MN-major
+};
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    wa_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                 const BwdParams prm) {
+  using C = DqCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const Smem sm = align_smem(smem_raw);
+  const uint32_t sQ = sm.base + C::kQOff, sDO = sm.base + C::kDOOff, sK = sm.base + C::kKOff, sV = sm.base + C::kVOff;
+  const uint32_t bar = sm.base + C::kBarOff;
+  const uint32_t b_qfull = bar, b_qempty = bar + 8, b_dpfree = bar + 48, b_ofull = bar + 56, b_drain = bar + 64;
+  auto b_sfull = [&](uint32_t n) { return bar + 16 + 8 * (n & 1); };
+  auto b_pfull = [&](uint32_t n) { return bar + 32 + 8 * (n & 1); };
+  auto b_kfull = [&](uint32_t s) { return bar + 8 * (9 + s); };
+  auto b_kempty = [&](uint32_t s) { return bar + 8 * (9 + C::kKSlots + s); };
+  auto b_vfull = [&](uint32_t s) { return bar + 8 * (9 + 2 * C::kKSlots + s); };
+  auto b_vempty = [&](uint32_t s) { return bar + 8 * (9 + 2 * C::kKSlots + C::kVSlots + s); };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* err = prm.err;
+
+  if (tid == 0) {
+    mbar_init(b_qfull, 1);
+    mbar_init(b_qempty, 1);
+    for (uint32_t n = 0; n < 2; ++n) {
+      mbar_init(b_sfull(n), 1);
+      mbar_init(b_pfull(n), 4);  // one arrival per elementwise warp
+    }
+    mbar_init(b_dpfree, 4);
+    mbar_init(b_ofull, 1);
+    mbar_init(b_drain, 1);
+    for (int s = 0; s < C::kKSlots; ++s) {
+      mbar_init(b_kfull(s), 1);
+      mbar_init(b_kempty(s), 1);
+    }
+    for (int s = 0; s < C::kVSlots; ++s) {
+      mbar_init(b_vfull(s), 1);
+      mbar_init(b_vempty(s), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tR2 = tmem + 256, tR3 = tmem + 384;
+
+  if (warp == 5) {
+    // ---------------------------------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t k_n = 0, v_n = 0, q_n = 0;
+      bool ok = true, dropped = false;
+      for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+        const Item it = load_item(prm.items, idx);
+        const int b = it.bh / prm.H, h = it.bh % prm.H;
+        const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+        const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
+        const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+        for (int t = 0; t < ntq && ok; ++t) {
+          ok = mbar_wait(b_qempty, (q_n & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          if (!ok) break;
+          if ((prm.debug_flags & 2) && !dropped && blockIdx.x == 0) {
+            dropped = true;  // fault injection for the watchdog test: this sub-item's query tiles never arrive
+          } else {
+            mbar_arrive_expect_tx(b_qfull, 2 * C::kTileBytes);
+            load_tile<D>(sQ, &tm_q, b_qfull, h, it.q_lo + t * kTileRows, b);
+            load_tile<D>(sDO, &tm_do, b_qfull, h, it.q_lo + t * kTileRows, b);
+          }
+          q_n++;
+          for (int j = 0; j < nt && ok; ++j) {
+            int valid;
+            const int row = step_row(it, j, nt0, &valid);
+            const uint32_t ks = k_n % C::kKSlots, vs = v_n % C::kVSlots;
+            ok = mbar_wait(b_kempty(ks), ((k_n / C::kKSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            if (!ok) break;
+            mbar_arrive_expect_tx(b_kfull(ks), C::kTileBytes);
+            load_tile<D>(sK + ks * C::kTileBytes, &tm_k, b_kfull(ks), h, row, b);
+            k_n++;
+            ok = mbar_wait(b_vempty(vs), ((v_n / C::kVSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            if (!ok) break;
+            mbar_arrive_expect_tx(b_vfull(vs), C::kTileBytes);
+            load_tile<D>(sV + vs * C::kTileBytes, &tm_v, b_vfull(vs), h, row, b);
+            v_n++;
+          }
+        }
+      }
+      if (!ok) {  // let the copies already issued land before the CTA's shared memory goes away
+        for (uint32_t n = k_n > (uint32_t)C::kKSlots ? k_n - C::kKSlots : 0; n < k_n; ++n)
+          mbar_wait_drain(b_kfull(n % C::kKSlots), (n / C::kKSlots) & 1, kDrainLimitNs);
+        for (uint32_t n = v_n > (uint32_t)C::kVSlots ? v_n - C::kVSlots : 0; n < v_n; ++n)
+          mbar_wait_drain(b_vfull(n % C::kVSlots), (n / C::kVSlots) & 1, kDrainLimitNs);
+        if (q_n) mbar_wait_drain(b_qfull, (q_n - 1) & 1, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t k_n = 0, v_n = 0, q_n = 0, dpf_n = 0, gs = 0;  // gs: steps of all earlier sub-items
+      bool ok = true;
+      const uint64_t dq_ = sdesc_sw128(sQ, 16, 1024), ddo = sdesc_sw128(sDO, 16, 1024);
+      const uint64_t dk_ = sdesc_sw128(sK, 16, 1024), dv_ = sdesc_sw128(sV, 16, 1024);
+      const uint64_t dk_mn = sdesc_sw128(sK, kTileRows * 128, 1024);  // key tiles as the MN-major B of dS.K
+      const uint32_t hi = (uint32_t)(dq_ >> 32);                      // common high word of every descriptor
+      // acc[tmem] = A B^T over the head dimension, both K-major (S = Q K^T, dP = dout V^T)
+      auto issue_nt = [&](uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * kTileRows * 128 + (kk % 4) * 32) >> 4;
+          mma_ss(d_tmem, a_lo + off, b_lo + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+        const Item it = load_item(prm.items, idx);
+        const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+        const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
+        for (int t = 0; t < ntq && ok; ++t) {
+          ok = mbar_wait(b_qfull, q_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          q_n++;
+          uint32_t kcur = k_n % C::kKSlots;
+          ok = ok && mbar_wait(b_kfull(kcur), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          k_n++;
+          uint32_t vs = v_n % C::kVSlots;
+          ok = ok && mbar_wait(b_vfull(vs), (v_n / C::kVSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          v_n++;
+          if (!ok) break;
+          tc_fence_after();
+          issue_nt(tmem + 128 * (gs & 1), (uint32_t)dq_, (uint32_t)dk_ + ((kcur * C::kTileBytes) >> 4));
+          issue_nt(tR2, (uint32_t)ddo, (uint32_t)dv_ + ((vs * C::kTileBytes) >> 4));
+          mma_commit(b_sfull(gs));
+          mma_commit(b_vempty(vs));
+          if (nt == 1) mma_commit(b_qempty);
+          for (int j = 0; j < nt && ok; ++j) {
+            const uint32_t n = gs + j;
+            uint32_t knext = 0;
+            if (j + 1 < nt) {
+              knext = k_n % C::kKSlots;
+              ok = mbar_wait(b_kfull(knext), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              k_n++;
+              if (!ok) break;
+              tc_fence_after();
+              issue_nt(tmem + 128 * ((n + 1) & 1), (uint32_t)dq_, (uint32_t)dk_ + ((knext * C::kTileBytes) >> 4));
+              ok = mbar_wait(b_dpfree, dpf_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dP(n) read
+              dpf_n++;
+              vs = v_n % C::kVSlots;
+              ok = ok && mbar_wait(b_vfull(vs), (v_n / C::kVSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              v_n++;
+              if (!ok) break;
+              tc_fence_after();
+              issue_nt(tR2, (uint32_t)ddo, (uint32_t)dv_ + ((vs * C::kTileBytes) >> 4));
+              mma_commit(b_sfull(n + 1));
+              mma_commit(b_vempty(vs));
+              if (j + 1 == nt - 1) mma_commit(b_qempty);  // every MMA that reads Q or dout has been issued
+            }
+            ok = mbar_wait(b_pfull(n), (n >> 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS(n) in TMEM
+            if (!ok) break;
+            tc_fence_after();
+            // dq += dS(n) K_n: dS from TMEM (first 64 columns of R[n % 2], 16 keys per MMA), K_n MN-major
+            const uint32_t kb = (uint32_t)dk_mn + ((kcur * C::kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kTileRows / 16; ++kk)
+              mma_ts(tR3, tmem + 128 * (n & 1) + kk * 8, kb + ((kk * 2048) >> 4), hi, C::kIdescDQ,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(b_kempty(kcur));
+            kcur = knext;
+          }
+          if (!ok) break;
+          ok = mbar_wait(b_dpfree, dpf_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // the last step's dP
+          dpf_n++;
+          if (!ok) break;
+          mma_commit(b_ofull);
+          gs += nt;
+        }
+      }
+      mma_commit(b_drain);
+      mbar_wait_drain(b_drain, 0, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    // ---------------------------------------------------------------------------------------- elementwise
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint32_t o_n = 0, gs = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+      const Item it = load_item(prm.items, idx);
+      const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+      const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
+      const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+      for (int t = 0; t < ntq && ok; ++t) {
+        const int row = it.q_lo + t * kTileRows + tid;
+        const bool in_seq = row < prm.L;
+        const float lse2 = in_seq ? __ldg(prm.lse + (int64_t)it.bh * prm.L + row) * kLog2e : 0.f;
+        const float drow = in_seq ? __ldg(prm.dvec + (int64_t)it.bh * prm.L + row) : 0.f;
+        for (int j = 0; j < nt; ++j) {
+          const uint32_t n = gs + j;
+          int valid;
+          step_row(it, j, nt0, &valid);
+          ok = mbar_wait(b_sfull(n), (n >> 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t dpr[128];
+          tmem_ld_x128(tR2 + lane_base, dpr);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_dpfree);
+          const uint32_t tS = tmem + lane_base + 128 * (n & 1);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t sr[32], pk[16];
+            tmem_ld_x32(tS + 32 * q4, sr);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int c0 = 32 * q4 + 2 * c;
+              const float p0 = c0 < valid ? ex2(fmaf(__uint_as_float(sr[2 * c]), prm.c_log2, -lse2)) : 0.f;
+              const float p1 = c0 + 1 < valid ? ex2(fmaf(__uint_as_float(sr[2 * c + 1]), prm.c_log2, -lse2)) : 0.f;
+              pk[c] = pack_bf16(p0 * (__uint_as_float(dpr[c0]) - drow), p1 * (__uint_as_float(dpr[c0 + 1]) - drow));
+            }
+            tmem_st_x16(tS + 16 * q4, pk);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_pfull(n));
+        }
+        if (!ok) break;
+        ok = mbar_wait(b_ofull, o_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        o_n++;
+        if (!ok) break;
+        tc_fence_after();
+        const bool row_ok = row < it.q_hi;
+        const int b = it.bh / prm.H, h = it.bh % prm.H;
+        if (it.split < 0) {
+          store_row<D>(tR3 + lane_base, prm.scale, row_ok,
+                       prm.dq + (int64_t)b * prm.sb + (int64_t)row * prm.sl + (int64_t)h * prm.sh, nullptr);
+        } else {
+          const int64_t slot = ((int64_t)it.bh * prm.G + (row - prm.g0)) * prm.n_splits + it.split;
+          store_row<D>(tR3 + lane_base, prm.scale, row_ok, nullptr, prm.ws_dq + slot * D);
+        }
+        tc_fence_before();
+        gs += nt;
+      }
+    }
+  }
+  teardown(tmem, warp);
+}
+
+// =====================================================================================================================
+// dk / dv kernel: key-major. Item rows are read as keys (one 128-key tile per sub-item, resident for the sub-item)
+// and the item's segments as the queries that keep them, streamed one 128-query tile per step.
+//   warps 0-3  elementwise: one thread per key (TMEM lane). Phase A: P^T = 2^(s c' - lse'_col) -> bf16 into TMEM.
+//              Phase B: dS^T = P^T (dP^T - Dvec_col) -> bf16 into TMEM. P stays in fp32 registers between them.
+//   warp 4     MMA issuer: S^T = K Q^T, dP^T = V dout^T, dv += P^T dout, dk += dS^T Q
+//   warp 5     loads (all lanes): lane 0 issues the TMA copies (the key / value tiles of the sub-item and a ring of
+//              query / dout tiles); every lane then stages 4 query columns' (lse, Dvec) into the ring slot.
+// TMEM: S^T [0,128) (P^T over its first 64 columns), dP^T [128,256) (dS^T over its first 64), dv [256, 256+D),
+// dk [384, 384+D). Issue order per step n: dv(n) after P^T(n) is written, then S^T(n+1); dk(n) after dS^T(n), then
+// dP^T(n+1). So the tensor core computes dv(n) and S^T(n+1) while the elementwise warps work on dS^T(n), and dk(n)
+// and dP^T(n+1) while they start P^T(n+1).
+// =====================================================================================================================
+template <int D>
+struct DkvCfg {
+  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kQSlots = D == 128 ? 2 : 3;  // ring of (query tile, dout tile, column values)
+  static constexpr int kSlotBytes = 2 * kTileBytes;
+  static constexpr int kKOff = 0, kVOff = kTileBytes;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kColOff = kRingOff + kQSlots * kSlotBytes;  // per slot: 64 x float4 {lse'_c, lse'_c+1, D_c, D_c+1}
+  static constexpr int kColBytes = 64 * 16;
+  static constexpr int kBarOff = kColOff + kQSlots * kColBytes;
+  // kv_full, kv_empty, s_full, p_full, dp_full, ds_full, o_full, drain, then q_full[slots], q_empty[slots]
+  static constexpr int kNumBars = 8 + 2 * kQSlots;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
+  static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 0, 1);  // A from TMEM, query-side tile MN-major
+};
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    wa_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams prm) {
+  using C = DkvCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const Smem sm = align_smem(smem_raw);
+  const uint32_t sK = sm.base + C::kKOff, sV = sm.base + C::kVOff, sRing = sm.base + C::kRingOff;
+  const uint32_t bar = sm.base + C::kBarOff;
+  const uint32_t b_kvfull = bar, b_kvempty = bar + 8, b_sfull = bar + 16, b_pfull = bar + 24, b_dpfull = bar + 32,
+                 b_dsfull = bar + 40, b_ofull = bar + 48, b_drain = bar + 56;
+  auto b_qfull = [&](uint32_t s) { return bar + 8 * (8 + s); };
+  auto b_qempty = [&](uint32_t s) { return bar + 8 * (8 + C::kQSlots + s); };
+  float4* colbuf = reinterpret_cast<float4*>(sm.p + C::kColOff);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* err = prm.err;
+
+  if (tid == 0) {
+    mbar_init(b_kvfull, 1);
+    mbar_init(b_kvempty, 1);
+    mbar_init(b_sfull, 1);
+    mbar_init(b_pfull, 4);
+    mbar_init(b_dpfull, 1);
+    mbar_init(b_dsfull, 4);
+    mbar_init(b_ofull, 1);
+    mbar_init(b_drain, 1);
+    for (int s = 0; s < C::kQSlots; ++s) {
+      mbar_init(b_qfull(s), 1 + 32);  // the copies' expect-tx arrival + one per loader lane (column values)
+      mbar_init(b_qempty(s), 1 + 4);  // the MMA commit + one per elementwise warp (column values read)
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
+
+  if (warp == 5) {
+    // ------------------------------------------------------------------------------------------- loaders
+    uint32_t kv_n = 0, q_n = 0;
+    bool ok = true, dropped = false;
+    for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+      const Item it = load_item(prm.items, idx);
+      const int b = it.bh / prm.H, h = it.bh % prm.H;
+      const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+      const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
+      const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+      const float* lse_bh = prm.lse + (int64_t)it.bh * prm.L;
+      const float* dv_bh = prm.dvec + (int64_t)it.bh * prm.L;
+      for (int t = 0; t < ntk && ok; ++t) {
+        ok = mbar_wait(b_kvempty, (kv_n & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(b_kvfull, 2 * C::kTileBytes);
+          load_tile<D>(sK, &tm_k, b_kvfull, h, it.q_lo + t * kTileRows, b);
+          load_tile<D>(sV, &tm_v, b_kvfull, h, it.q_lo + t * kTileRows, b);
+        }
+        kv_n++;
+        for (int j = 0; j < nt && ok; ++j) {
+          int valid;
+          const int row = step_row(it, j, nt0, &valid);
+          // this lane's 4 query columns: loads issued before the wait so that their latency hides behind it
+          float l4[4], d4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = 4 * lane + i;
+            l4[i] = c < valid ? __ldg(lse_bh + row + c) * kLog2e : 0.f;
+            d4[i] = c < valid ? __ldg(dv_bh + row + c) : 0.f;
+          }
+          const uint32_t qs = q_n % C::kQSlots;
+          ok = mbar_wait(b_qempty(qs), ((q_n / C::kQSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          if (lane == 0) {
+            if ((prm.debug_flags & 4) && !dropped && blockIdx.x == 0) {
+              dropped = true;  // fault injection for the watchdog test: bytes expected, no copy issued
+              mbar_arrive_expect_tx(b_qfull(qs), C::kSlotBytes);
+            } else {
+              const uint32_t dst = sRing + qs * C::kSlotBytes;
+              mbar_arrive_expect_tx(b_qfull(qs), C::kSlotBytes);
+              load_tile<D>(dst, &tm_q, b_qfull(qs), h, row, b);
+              load_tile<D>(dst + C::kTileBytes, &tm_do, b_qfull(qs), h, row, b);
+            }
+          }
+          float4* cb = colbuf + qs * 64 + 2 * lane;
+          cb[0] = make_float4(l4[0], l4[1], d4[0], d4[1]);
+          cb[1] = make_float4(l4[2], l4[3], d4[2], d4[3]);
+          mbar_arrive(b_qfull(qs));  // release: the column values are visible to whoever waits on q_full
+          q_n++;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      if (kv_n) mbar_wait_drain(b_kvfull, (kv_n - 1) & 1, kDrainLimitNs);
+      for (uint32_t n = q_n > (uint32_t)C::kQSlots ? q_n - C::kQSlots : 0; n < q_n; ++n)
+        mbar_wait_drain(b_qfull(n % C::kQSlots), (n / C::kQSlots) & 1, kDrainLimitNs);
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kv_n = 0, q_n = 0, p_n = 0, ds_n = 0;
+      bool ok = true;
+      const uint64_t dk_ = sdesc_sw128(sK, 16, 1024), dv_ = sdesc_sw128(sV, 16, 1024);
+      const uint64_t dr_k = sdesc_sw128(sRing, 16, 1024);                // ring tiles as K-major B (S^T, dP^T)
+      const uint64_t dr_mn = sdesc_sw128(sRing, kTileRows * 128, 1024);  // ring tiles as MN-major B (dv, dk)
+      const uint32_t hi = (uint32_t)(dk_ >> 32);
+      auto issue_nt = [&](uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * kTileRows * 128 + (kk % 4) * 32) >> 4;
+          mma_ss(d_tmem, a_lo + off, b_lo + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      // acc (+)= A[tmem: 128 keys x 128 queries, bf16] . B[smem: 128 queries x D], 16 queries per MMA
+      auto issue_acc = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_ts(d_tmem, a_tmem + kk * 8, b_lo + ((kk * 2048) >> 4), hi, C::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
+      };
+      auto slot_k = [&](uint32_t s, uint32_t tile) { return (uint32_t)dr_k + ((s * C::kSlotBytes + tile) >> 4); };
+      auto slot_mn = [&](uint32_t s, uint32_t tile) { return (uint32_t)dr_mn + ((s * C::kSlotBytes + tile) >> 4); };
+      for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+        const Item it = load_item(prm.items, idx);
+        const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+        const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
+        for (int t = 0; t < ntk && ok; ++t) {
+          ok = mbar_wait(b_kvfull, kv_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          kv_n++;
+          uint32_t qs = q_n % C::kQSlots;
+          ok = ok && mbar_wait(b_qfull(qs), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          q_n++;
+          if (!ok) break;
+          tc_fence_after();
+          issue_nt(tS, (uint32_t)dk_, slot_k(qs, 0));  // S^T(0) = K Q_0^T
+          mma_commit(b_sfull);
+          issue_nt(tDP, (uint32_t)dv_, slot_k(qs, C::kTileBytes));  // dP^T(0) = V dout_0^T
+          mma_commit(b_dpfull);
+          if (nt == 1) mma_commit(b_kvempty);
+          for (int j = 0; j < nt && ok; ++j) {
+            ok = mbar_wait(b_pfull, p_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // P^T(j) in TMEM
+            p_n++;
+            if (!ok) break;
+            tc_fence_after();
+            issue_acc(tDV, tS, slot_mn(qs, C::kTileBytes), j > 0);  // dv += P^T(j) dout_j
+            uint32_t qn = 0;
+            if (j + 1 < nt) {
+              qn = q_n % C::kQSlots;
+              ok = mbar_wait(b_qfull(qn), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              q_n++;
+              if (!ok) break;
+              tc_fence_after();
+              issue_nt(tS, (uint32_t)dk_, slot_k(qn, 0));  // S^T(j+1)
+              mma_commit(b_sfull);
+            }
+            ok = mbar_wait(b_dsfull, ds_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS^T(j) in TMEM
+            ds_n++;
+            if (!ok) break;
+            tc_fence_after();
+            issue_acc(tDK, tDP, slot_mn(qs, 0), j > 0);  // dk += dS^T(j) Q_j
+            mma_commit(b_qempty(qs));
+            if (j + 1 < nt) {
+              issue_nt(tDP, (uint32_t)dv_, slot_k(qn, C::kTileBytes));  // dP^T(j+1)
+              mma_commit(b_dpfull);
+              if (j + 1 == nt - 1) mma_commit(b_kvempty);  // every MMA that reads the key / value tiles is issued
+            }
+            qs = qn;
+          }
+          if (!ok) break;
+          mma_commit(b_ofull);
+        }
+      }
+      mma_commit(b_drain);
+      mbar_wait_drain(b_drain, 0, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    // ---------------------------------------------------------------------------------------- elementwise
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint32_t q_n = 0, s_n = 0, o_n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+      const Item it = load_item(prm.items, idx);
+      const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+      const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
+      const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+      for (int t = 0; t < ntk && ok; ++t) {
+        for (int j = 0; j < nt; ++j) {
+          int valid;
+          step_row(it, j, nt0, &valid);
+          const uint32_t qs = q_n % C::kQSlots;
+          ok = mbar_wait(b_qfull(qs), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = ok && mbar_wait(b_sfull, s_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          q_n++;
+          if (!ok) break;
+          tc_fence_after();
+          const float4* cb = colbuf + qs * 64;
+          // Phase A: P^T = 2^(s c' - lse'_col) over this key's 128 query columns (columns past the segment: 0)
+          float p[128];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t sr[32], pk[16];
+            tmem_ld_x32(tS + lane_base + 32 * q4, sr);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int c0 = 32 * q4 + 2 * c;
+              const float4 cv = cb[c0 >> 1];
+              p[c0] = c0 < valid ? ex2(fmaf(__uint_as_float(sr[2 * c]), prm.c_log2, -cv.x)) : 0.f;
+              p[c0 + 1] = c0 + 1 < valid ? ex2(fmaf(__uint_as_float(sr[2 * c + 1]), prm.c_log2, -cv.y)) : 0.f;
+              pk[c] = pack_bf16(p[c0], p[c0 + 1]);
+            }
+            tmem_st_x16(tS + lane_base + 16 * q4, pk);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_pfull);
+          // Phase B: dS^T = P^T (dP^T - Dvec_col)
+          ok = mbar_wait(b_dpfull, s_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          s_n++;
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t dr[32], pk[16];
+            tmem_ld_x32(tDP + lane_base + 32 * q4, dr);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int c0 = 32 * q4 + 2 * c;
+              const float4 cv = cb[c0 >> 1];
+              pk[c] = pack_bf16(p[c0] * (__uint_as_float(dr[2 * c]) - cv.z),
+                                p[c0 + 1] * (__uint_as_float(dr[2 * c + 1]) - cv.w));
+            }
+            tmem_st_x16(tDP + lane_base + 16 * q4, pk);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(b_dsfull);
+            mbar_arrive(b_qempty(qs));  // this slot's column values are no longer needed
+          }
+        }
+        if (!ok) break;
+        ok = mbar_wait(b_ofull, o_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        o_n++;
+        if (!ok) break;
+        tc_fence_after();
+        const int key = it.q_lo + t * kTileRows + tid;
+        const bool row_ok = key < it.q_hi;
+        const int b = it.bh / prm.H, h = it.bh % prm.H;
+        if (it.split < 0) {
+          const int64_t off = (int64_t)b * prm.sb + (int64_t)key * prm.sl + (int64_t)h * prm.sh;
+          store_row<D>(tDV + lane_base, 1.f, row_ok, prm.dv + off, nullptr);
+          store_row<D>(tDK + lane_base, prm.scale, row_ok, prm.dk + off, nullptr);
+        } else {
+          const int64_t slot = (((int64_t)it.bh * prm.G + (key - prm.g0)) * prm.n_splits + it.split) * D;
+          store_row<D>(tDV + lane_base, 1.f, row_ok, nullptr, prm.ws_dv + slot);
+          store_row<D>(tDK + lane_base, prm.scale, row_ok, nullptr, prm.ws_dk + slot);
+        }
+        tc_fence_before();
+      }
+    }
+  }
+  teardown(tmem, warp);
+}
+
+// Dvec_i = dout_i . out_i for every (b, i, h), one warp per row, rows in memory order; fp32 into [B*H][L].
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dot_kernel(const __nv_bfloat16* __restrict__ out,
+                                                      const __nv_bfloat16* __restrict__ dout,
+                                                      float* __restrict__ dvec, int64_t rows, int L, int H,
+                                                      int64_t sb, int64_t sl, int64_t sh) {
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int h = (int)(r % H);
+  const int64_t bl = r / H;
+  const int l = (int)(bl % L), b = (int)(bl / L);
+  const int64_t off = (int64_t)b * sb + (int64_t)l * sl + (int64_t)h * sh;
+  constexpr int kPer = D / 32;  // elements per lane: 4 (8 bytes) or 2 (4 bytes)
+  float acc = 0.f;
+  if constexpr (kPer == 4) {
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>(out + off) + lane);
+    const uint2 g = __ldg(reinterpret_cast<const uint2*>(dout + off) + lane);
+    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+    const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+    const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
+    const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
+    acc = fmaf(a0.x, g0.x, fmaf(a0.y, g0.y, fmaf(a1.x, g1.x, a1.y * g1.y)));
+  } else {
+    const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(out + off) + lane);
+    const uint32_t g = __ldg(reinterpret_cast<const uint32_t*>(dout + off) + lane);
+    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+    const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g));
+    acc = fmaf(a0.x, g0.x, a0.y * g0.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) dvec[((int64_t)b * H + h) * L + l] = acc;
+}
+
+// Sum the split partials of the global rows into bf16 rows: tensor blockIdx.y (0 dq, 1 dk, 2 dv), one warp per row,
+// splits added in index order.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_sum_kernel(const float* __restrict__ ws, int64_t part_elems,
+                                                      __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
+                                                      int rows, int G, int H, int g0, int P, int64_t sb, int64_t sl,
+                                                      int64_t sh) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int which = blockIdx.y;
+  const float* src = ws + which * part_elems + (int64_t)r * P * D;
+  __nv_bfloat16* dst = which == 0 ? dq : (which == 1 ? dk : dv);
+  constexpr int kPer = D / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  for (int p = 0; p < P; ++p) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] += __ldg(src + (int64_t)p * D + lane + 32 * i);
+  }
+  const int bh = r / G, gr = r % G;
+  const int b = bh / H, h = bh % H;
+  __nv_bfloat16* d = dst + (int64_t)b * sb + (int64_t)(g0 + gr) * sl + (int64_t)h * sh;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) d[lane + 32 * i] = __float2bfloat16_rn(acc[i]);
+}
+
+template <int D>
+int launch_backward_d(const BackwardArgs& a, cudaStream_t s, int num_sms, void* const* events) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(wa_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqCfg<D>::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(wa_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DkvCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  const Geometry& g = *a.geo;
+  const wa_layout_t& l = g.layout;
+  alignas(64) CUtensorMap mq, mk, mv, mdo;
+  if (!make_tile_map(&mq, a.q, g, 2) || !make_tile_map(&mk, a.k, g, 2) || !make_tile_map(&mv, a.v, g, 2) ||
+      !make_tile_map(&mdo, a.dout, g, 2))
+    return (int)cudaErrorInvalidValue;
+  auto rec = [&](int i) { return events ? cudaEventRecord((cudaEvent_t)events[i], s) : cudaSuccess; };
+  cudaError_t e = rec(0);
+  if (e != cudaSuccess) return (int)e;
+  const int64_t rows = (int64_t)l.B * g.L * l.H;
+  bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(a.out), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.dvec, rows,
+      (int)g.L, l.H, l.stride_b, l.stride_l, l.stride_h);
+  if ((e = cudaGetLastError()) != cudaSuccess || (e = rec(1)) != cudaSuccess) return (int)e;
+  BwdParams p;
+  p.items = a.items;
+  p.n_items = a.n_items;
+  p.lse = a.lse;
+  p.dvec = a.dvec;
+  p.dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
+  p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
+  p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
+  p.ws_dq = a.ws;
+  p.ws_dk = a.ws ? a.ws + a.part_elems : nullptr;
+  p.ws_dv = a.ws ? a.ws + 2 * a.part_elems : nullptr;
+  p.err = a.err;
+  p.sb = l.stride_b;
+  p.sl = l.stride_l;
+  p.sh = l.stride_h;
+  p.H = l.H;
+  p.G = g.G;
+  p.g0 = (int)g.g0;
+  p.L = (int)g.L;
+  p.n_splits = a.n_splits;
+  p.c_log2 = (float)(1.4426950408889634 / sqrt((double)D));
+  p.scale = (float)(1.0 / sqrt((double)D));
+  p.debug_flags = a.debug_flags;
+  const int grid = a.n_items < num_sms ? a.n_items : num_sms;
+  if (grid > 0) {
+    wa_dq_kernel<D><<<grid, kBwdThreads, DqCfg<D>::kSmemBytes, s>>>(mq, mk, mv, mdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  }
+  if ((e = rec(2)) != cudaSuccess) return (int)e;
+  if (grid > 0) {
+    wa_dkdv_kernel<D><<<grid, kBwdThreads, DkvCfg<D>::kSmemBytes, s>>>(mq, mk, mv, mdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  }
+  if ((e = rec(3)) != cudaSuccess) return (int)e;
+  if (g.G > 0) {
+    const int grows = l.B * l.H * g.G;
+    bwd_sum_kernel<D><<<dim3((grows + 7) / 8, 3), 256, 0, s>>>(a.ws, a.part_elems, p.dq, p.dk, p.dv, grows, g.G, l.H,
+                                                                (int)g.g0, a.n_splits, l.stride_b, l.stride_l,
+                                                                l.stride_h);
+    if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  }
+  return (int)rec(4);
+}
+
+}  // namespace
+
+int launch_backward(const BackwardArgs& a, void* stream, int num_sms, void* const* events) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return a.geo->layout.D == 128 ? launch_backward_d<128>(a, s, num_sms, events)
+                                : launch_backward_d<64>(a, s, num_sms, events);
+}
+
+}  // namespace wa

@@ -67,6 +67,36 @@ int launch_attention(const LaunchArgs& a, void* stream, int num_sms);
 // Launch the log-sum-exp merge of the global rows; returns a CUDA error code.
 int launch_combine(const LaunchArgs& a, void* stream);
 
+// Arguments of one backward pass (device pointers; every [B, L, H, D] tensor has the plan's strides).
+struct BackwardArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out;    // the forward's output
+  const void* dout;   // gradient of the loss with respect to out
+  const float* lse;   // [B][H][L] natural-log row log-sum-exp written by the forward
+  void* dq;
+  void* dk;
+  void* dv;
+  const Item* items;
+  int n_items;
+  float* dvec;        // [B*H][L] scratch: dout_i . out_i
+  float* ws;          // 3 x part_elems fp32 scratch: split partials of the global rows' dq, dk, dv
+  int64_t part_elems; // B*H*G*n_splits*D
+  int* err;
+  int n_splits;
+  int debug_flags;
+  const Geometry* geo;
+};
+
+// Launch the backward (row dot products, dq kernel, dk/dv kernel, split sums) on `stream`. `events`, when not null,
+// holds five CUDA events recorded before, between and after the four launches. Returns a CUDA error code.
+int launch_backward(const BackwardArgs& a, void* stream, int num_sms, void* const* events);
+
+// Encode the 4-D TMA map of a [B, L, H, D] tensor (box 128 bytes x 1 x 128 rows x 1, 128-byte swizzle) into
+// `map` (a 64-byte aligned CUtensorMap). elem_bytes 2: bf16, 1: 8-bit. Returns false if encoding fails.
+bool make_tile_map(void* map, const void* ptr, const Geometry& g, int elem_bytes);
+
 // Device error word bits.
 constexpr int kErrTimeout = 1;
 constexpr int kErrBounds = 2;

@@ -625,6 +625,10 @@ int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
 
 }  // namespace
 
+bool make_tile_map(void* map, const void* ptr, const Geometry& g, int elem_bytes) {
+  return make_map(reinterpret_cast<CUtensorMap*>(map), ptr, g, elem_bytes);
+}
+
 int launch_attention(const LaunchArgs& a, void* stream, int num_sms) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (a.qk_fp8) return a.geo->layout.D == 128 ? launch_attention_d<128, true>(a, s, num_sms) : (int)cudaErrorInvalidValue;

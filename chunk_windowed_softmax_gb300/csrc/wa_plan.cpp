@@ -38,6 +38,11 @@ struct wa_plan {
   bool profiling = false;
   int prof_n = 0;
   std::vector<cudaEvent_t> prof_ev;
+  // Backward workspace (allocated by the first wa_backward): row dot products, then the split partials of the
+  // global rows' dq, dk and dv. Five profiling events per recorded backward.
+  float* d_bws = nullptr;
+  int bprof_n = 0;
+  std::vector<cudaEvent_t> bprof_ev;
 };
 
 namespace wa {
@@ -189,9 +194,11 @@ void free_plan(wa_plan* p) {
   if (p->device >= 0 && cur != p->device) cudaSetDevice(p->device);
   if (p->d_items) cudaFree(p->d_items);
   if (p->d_ws) cudaFree(p->d_ws);
+  if (p->d_bws) cudaFree(p->d_bws);
   if (p->d_err) cudaFree(p->d_err);
   if (p->done) cudaEventDestroy(p->done);
   for (cudaEvent_t e : p->prof_ev) cudaEventDestroy(e);
+  for (cudaEvent_t e : p->bprof_ev) cudaEventDestroy(e);
   if (p->device >= 0 && cur >= 0 && cur != p->device) cudaSetDevice(cur);
   delete p;
 }
@@ -447,11 +454,98 @@ wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const 
   return forward_impl(plan, q8, k8, v, out, stream, 1, q_scale * k_scale);
 }
 
+wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void* v, const void* out, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, wa_stream_t stream) {
+  if (!plan || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return WA_ERR_INVALID;
+  auto al = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
+  if (!al(q) || !al(k) || !al(v) || !al(out) || !al(dout) || !al(dq) || !al(dk) || !al(dv) || ((uintptr_t)lse & 3))
+    return WA_ERR_INVALID;
+  const wa::Geometry& g = plan->hp.geo;
+  const wa_layout_t& l = g.layout;
+  const size_t span = 2 * (size_t)((l.B - 1) * l.stride_b + (g.L - 1) * l.stride_l + (l.H - 1) * l.stride_h + l.D);
+  const size_t lse_span = (size_t)4 * l.B * l.H * g.L;
+  const void* outs[3] = {dq, dk, dv};
+  const void* ins[6] = {q, k, v, out, dout, lse};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = i + 1; j < 3; ++j)
+      if (ranges_overlap((uintptr_t)outs[i], span, (uintptr_t)outs[j], span)) return WA_ERR_INVALID;
+    for (int j = 0; j < 6; ++j)
+      if (ranges_overlap((uintptr_t)outs[i], span, (uintptr_t)ins[j], j == 5 ? lse_span : span))
+        return WA_ERR_INVALID;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) {
+    cudaGetLastError();
+    return WA_ERR_INVALID;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  std::lock_guard<std::mutex> lk(plan->mu);
+  const int64_t BH = (int64_t)l.B * l.H;
+  const int64_t part = BH * g.G * plan->hp.n_splits * l.D;
+  // The partials are written with 16-byte vector stores: start them on a 256-byte boundary after the row dots.
+  const int64_t dvec_elems = (BH * g.L + 63) / 64 * 64;
+  if (!plan->d_bws) {
+    const size_t bytes = (size_t)(dvec_elems + 3 * part) * sizeof(float);
+    if (dev_alloc(&plan->d_bws, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      plan->d_bws = nullptr;
+      return WA_ERR_OOM;
+    }
+  }
+  if (plan->have_last && plan->last_stream != s) {
+    if (cudaStreamWaitEvent(s, plan->done, 0) != cudaSuccess) return WA_ERR_CUDA;
+  }
+  wa::BackwardArgs a;
+  a.q = q; a.k = k; a.v = v; a.out = out; a.dout = dout; a.lse = lse;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.items = plan->d_items;
+  a.n_items = (int)plan->hp.items.size();
+  a.dvec = plan->d_bws;
+  a.ws = plan->d_bws + dvec_elems;
+  a.part_elems = part;
+  a.err = plan->d_err;
+  a.n_splits = plan->hp.n_splits;
+  a.debug_flags = plan->debug_flags;
+  a.geo = &g;
+  void* const* ev = nullptr;
+  if (plan->profiling && plan->bprof_n < kMaxProfiled) {
+    while ((int)plan->bprof_ev.size() < 5 * (plan->bprof_n + 1)) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return WA_ERR_CUDA;
+      plan->bprof_ev.push_back(e);
+    }
+    ev = reinterpret_cast<void* const*>(&plan->bprof_ev[5 * plan->bprof_n++]);
+  }
+  if (wa::launch_backward(a, (void*)s, plan->num_sms, ev) != 0) return WA_ERR_CUDA;
+  if (cudaEventRecord(plan->done, s) != cudaSuccess) return WA_ERR_CUDA;
+  plan->last_stream = s;
+  plan->have_last = true;
+  return WA_OK;
+}
+
 int wa_plan_profile(wa_plan_t* plan, int enable) {
   if (!plan) return WA_ERR_INVALID;
   std::lock_guard<std::mutex> lk(plan->mu);
   plan->profiling = enable != 0;
   plan->prof_n = 0;
+  plan->bprof_n = 0;
+  return WA_OK;
+}
+
+int wa_plan_profile_read_backward(wa_plan_t* plan, double* ms, int* n_backwards) {
+  if (!plan || !ms || !n_backwards) return WA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(plan->mu);
+  for (int k = 0; k < 4; ++k) ms[k] = 0.0;
+  *n_backwards = plan->bprof_n;
+  for (int i = 0; i < plan->bprof_n; ++i) {
+    cudaEvent_t* ev = &plan->bprof_ev[5 * i];
+    if (cudaEventSynchronize(ev[4]) != cudaSuccess) return WA_ERR_CUDA;
+    for (int k = 0; k < 4; ++k) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, ev[k], ev[k + 1]) != cudaSuccess) return WA_ERR_CUDA;
+      ms[k] += t;
+    }
+  }
   return WA_OK;
 }
 

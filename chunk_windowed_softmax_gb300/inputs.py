@@ -6,7 +6,8 @@ float32 N(0, 1) of shape [B, L, H, D]; when ``k_global_scale`` is not 1 the keys
 multiplied by it (x2 is exact in bf16); every tensor is then cast to bfloat16. Draws on a CUDA device use
 torch's Philox generator there (milliseconds even at H3 scale); draws on the CPU use torch's CPU generator.
 The two devices give different values for the same seed, so a comparison always reads the oracle's inputs back
-from the very tensors the GPU used.
+from the very tensors the GPU used. The backward's upstream gradient dout is drawn the same way from its own
+generator, seeded with the workload's seed + 7919, as float32 N(0, 1) cast to bfloat16.
 """
 import torch
 
@@ -25,3 +26,12 @@ def make_qkv(w, seed=None, device="cpu"):
         out.append(x.to(torch.bfloat16).contiguous())
         del x
     return tuple(out)
+
+
+def make_dout(w, seed=None, device="cpu"):
+    """Return dout, a contiguous bf16 tensor of shape [B, L, H, D]: the upstream gradient for workload ``w``."""
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed((w.seed if seed is None else seed) + 7919)
+    x = torch.randn((w.B, w.L, w.H, w.D), generator=g, dtype=torch.float32, device=device)
+    return x.to(torch.bfloat16).contiguous()

@@ -126,6 +126,26 @@ wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const 
                          float k_scale, wa_stream_t stream);
 
 /*
+ * Gradients of a scalar loss through the forward: given dout = d(loss)/d(out), writes
+ *   dq = d(loss)/dq, dk = d(loss)/dk, dv = d(loss)/dv
+ * for the same kept sets as wa_forward (VDN-Minimax-H3 window-attention article, section 一 for the kept sets and
+ * section 三 for the softmax restricted to them; the chain rule through that softmax, per row i with kept set J:
+ * dv_j += P_ij dout_i, dS_ij = P_ij (dout_i.v_j - dout_i.out_i), dq_i = sum_j dS_ij k_j / sqrt(D),
+ * dk_j += dS_ij q_i / sqrt(D)).
+ *   q, k, v, out, dout, dq, dk, dv: device pointers to bf16 [B, L, H, D] with the plan's element strides,
+ *     16-byte aligned. out and lse must be what wa_forward_lse wrote for these q, k, v (the probabilities are
+ *     recomputed from lse, not stored). Every element of dq, dk, dv is written.
+ *   lse: device fp32 [B][H][L] contiguous, 4-byte aligned.
+ * Ordering: as wa_forward (calls on one plan are ordered across streams by the library). The first call on a plan
+ * allocates its backward workspace: B*H*L*4 (rounded up to 256) + 3*B*H*G*n_splits*D*4 bytes, kept until the plan is freed.
+ * Errors (synchronous, nothing launched): WA_ERR_INVALID for null or misaligned pointers, or when dq, dk or dv
+ * overlaps each other or any input; WA_ERR_OOM when the workspace cannot be allocated; WA_ERR_CUDA when a launch
+ * fails. Device-side failures: see wa_plan_check_error().
+ */
+wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void* v, const void* out, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, wa_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the plan's device error word.
  * Returns WA_OK, WA_ERR_DEVICE_TIMEOUT, WA_ERR_DEVICE_BOUNDS, or WA_ERR_CUDA if the synchronisation failed.
  */
@@ -176,8 +196,9 @@ wa_status wa_forward_static(int T, int S, int K, int r, int G, const wa_layout_t
 /*
  * Fault injection for the watchdog test. flags & 1: the next forward's producer skips one key-tile copy, so the
  * consumer's bounded wait runs out (about 2 s), the kernel unwinds and latches WA_ERR_DEVICE_TIMEOUT, which
- * wa_plan_check_error() then reports. The device stays usable; later forwards with flags == 0 are correct.
- * Returns WA_ERR_INVALID for a NULL plan.
+ * wa_plan_check_error() then reports. flags & 2 and flags & 4 do the same to the backward's dq kernel and dk/dv
+ * kernel (one query-tile copy is never issued). The device stays usable; later calls with flags == 0 are
+ * correct. Returns WA_ERR_INVALID for a NULL plan.
  */
 int wa_plan_set_debug_flags(wa_plan_t* plan, int flags);
 
@@ -190,6 +211,11 @@ int wa_plan_set_debug_flags(wa_plan_t* plan, int flags);
  */
 int wa_plan_profile(wa_plan_t* plan, int enable);
 int wa_plan_profile_read(wa_plan_t* plan, double* attention_ms, double* combine_ms, int* n_forwards);
+/*
+ * The same for the backward passes recorded while profiling is enabled (up to 4096): ms[0..3] receive the summed
+ * device time of the row dot products, the dq kernel, the dk/dv kernel and the split sums; *n_backwards the count.
+ */
+int wa_plan_profile_read_backward(wa_plan_t* plan, double* ms, int* n_backwards);
 
 /* Number of plans currently held by the cache (referenced or not). */
 int wa_cache_size(void);

@@ -42,3 +42,123 @@ def test_forward_lse_full(cuda, w):
     want = ref.row_logsumexp(q, k, w.T, w.S, w.K, w.r, w.G, w.global_pos)
     err = np.abs(got - want).max()
     assert err <= LSE_TOL, f"{w.name}: max |lse error| {err:.3e}"
+
+
+# --------------------------------------------------------------------------------------------------- gradients
+GRAD_REL = 1e-2
+GRAD_ABS = 5e-2  # times max |reference| of the slice
+
+
+def gpu_backward(wa, w, q, k, v, dout):
+    plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    try:
+        out, lse = plan.forward_lse(q, k, v)
+        dq, dk, dv = plan.backward(q, k, v, out, dout, lse)
+        assert plan.check_error() == 0
+    finally:
+        plan.close()
+    return dq, dk, dv
+
+
+def check_grads(got, want, label):
+    """got: (dq, dk, dv) GPU tensors; want: float64 arrays. The bar applies per (b, h) slice and tensor."""
+    worst = {}
+    for name, g, r in zip(("dq", "dk", "dv"), got, want):
+        g = g.float().cpu().double().numpy()
+        for b in range(r.shape[0]):
+            for h in range(r.shape[2]):
+                gs, rs = g[b, :, h], r[b, :, h]
+                rel = np.linalg.norm(gs - rs) / max(np.linalg.norm(rs), 1e-30)
+                ab = np.abs(gs - rs).max() / max(np.abs(rs).max(), 1e-30)
+                wr, wa_ = worst.get(name, (0.0, 0.0))
+                worst[name] = (max(wr, rel), max(wa_, ab))
+    msg = ", ".join(f"{n}: rel {a:.2e} abs {b:.2e}" for n, (a, b) in worst.items())
+    print(f"{label}: {msg}")
+    for n, (rel, ab) in worst.items():
+        assert rel <= GRAD_REL and ab <= GRAD_ABS, f"{label} {n}: {msg}"
+
+
+GRAD_CASES = [
+    configs.TINY,
+    configs.MEDIUM,
+    configs.Workload("bwd_ragged", B=2, H=2, D=128, T=50, S=60, K=4, r=2, G=77, global_pos=1, seed=41),
+    configs.Workload("bwd_no_globals", B=1, H=2, D=128, T=9, S=100, K=2, r=1, G=0, global_pos=0, seed=42),
+    configs.Workload("bwd_many_splits", B=1, H=2, D=128, T=40, S=64, K=1, r=0, G=300, global_pos=0, seed=43),
+    configs.Workload("bwd_d64_front", B=2, H=2, D=64, T=13, S=37, K=4, r=2, G=130, global_pos=1, seed=44),
+    configs.Workload("bwd_one_token_frames", B=1, H=2, D=128, T=300, S=1, K=7, r=2, G=5, global_pos=1, seed=45),
+    configs.Workload("bwd_single_row", B=1, H=1, D=128, T=1, S=1, K=1, r=0, G=0, global_pos=0, seed=46),
+    configs.Workload("bwd_radius_covers_all", B=1, H=2, D=128, T=7, S=90, K=2, r=9, G=40, global_pos=0, seed=47),
+    configs.Workload("bwd_sharp_globals", B=1, H=2, D=128, T=12, S=64, K=3, r=1, G=256, global_pos=0, seed=48,
+                     k_global_scale=4.0),
+]
+
+
+@pytest.mark.parametrize("w", GRAD_CASES, ids=lambda w: w.name)
+def test_backward_full(cuda, w):
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    got = gpu_backward(cuda, w, q, k, v, dout)
+    want = ref.window_attention_backward(q, k, v, dout, w.T, w.S, w.K, w.r, w.G, w.global_pos)
+    check_grads(got, want, w.name)
+
+
+def test_backward_deterministic_and_streams(cuda):
+    w = configs.MEDIUM
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    try:
+        out, lse = plan.forward_lse(q, k, v)
+        a = plan.backward(q, k, v, out, dout, lse)
+        s2 = torch.cuda.Stream()
+        with torch.cuda.stream(s2):
+            b = plan.backward(q, k, v, out, dout, lse)
+        torch.cuda.synchronize()
+        assert plan.check_error() == 0
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    finally:
+        plan.close()
+
+
+def test_backward_matches_autograd_of_dense_masked_attention(cuda):
+    """Independent of the oracle's loop: torch autograd (float64, CPU) through dense attention with the kept-set
+    mask built by brute force from the chunk rule."""
+    w = configs.Workload("bwd_dense", B=1, H=2, D=64, T=8, S=20, K=2, r=1, G=24, global_pos=0, seed=49)
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    got = gpu_backward(cuda, w, q, k, v, dout)
+    L = w.L
+    chunk = [(i // w.S) // w.K if i < w.F else -1 for i in range(L)]
+    mask = torch.zeros(L, L, dtype=torch.bool)
+    for i in range(L):
+        for j in range(L):
+            mask[i, j] = chunk[i] < 0 or chunk[j] < 0 or abs(chunk[i] - chunk[j]) <= w.r
+    qd, kd, vd = (t.double().cpu().requires_grad_(True) for t in (q, k, v))
+    s = torch.einsum("blhd,bmhd->bhlm", qd, kd) / np.sqrt(w.D)
+    p = torch.softmax(s.masked_fill(~mask, float("-inf")), dim=-1)
+    o = torch.einsum("bhlm,bmhd->blhd", p, vd)
+    (o * dout.double().cpu()).sum().backward()
+    check_grads(got, [t.grad.numpy() for t in (qd, kd, vd)], "dense autograd")
+
+
+@pytest.mark.parametrize("flag", [2, 4], ids=["dq_kernel", "dkdv_kernel"])
+def test_backward_watchdog(cuda, flag):
+    """A copy that never arrives: the bounded wait expires, the kernel unwinds and the error is reported; the next
+    backward on the same plan is correct."""
+    w = configs.Workload("bwd_watchdog", B=1, H=2, D=128, T=6, S=64, K=2, r=1, G=32, global_pos=0, seed=50)
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    try:
+        out, lse = plan.forward_lse(q, k, v)
+        plan.set_debug_flags(flag)
+        plan.backward(q, k, v, out, dout, lse)
+        assert plan.check_error() == 5  # WA_ERR_DEVICE_TIMEOUT
+        plan.set_debug_flags(0)
+        got = plan.backward(q, k, v, out, dout, lse)
+        assert plan.check_error() == 0
+    finally:
+        plan.close()
+    want = ref.window_attention_backward(q, k, v, dout, w.T, w.S, w.K, w.r, w.G, w.global_pos)
+    check_grads(got, want, "after watchdog")
