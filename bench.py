@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--fp8", action="store_true",
                     help="time wa_forward_fp8 (e4m3 queries / keys, per-tensor scales; bf16 values and output)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (dq, dk, dv through wa_backward) instead of the forward")
     ap.add_argument("--sweep", action="store_true",
                     help="auxiliary: one JSON line per sweep point (kept TFLOP/s vs window density), 1 GPU")
     return ap.parse_args()
@@ -260,10 +262,70 @@ def run_sweep(args):
         del q, k, v, out
 
 
+def run_backward(args, w):
+    """Backward throughput on one GPU: each step is one wa_backward (row dots, dq kernel, dk/dv kernel, split sums)
+    on device-resident q, k, v, out, dout and lse from one forward. Useful work is counted as the five products of
+    the chain rule per kept pair (S, dP, dv, dk, dq: 10 D flops); the kernels recompute S and dP once more."""
+    import torch
+    import chunk_windowed_softmax_gb300 as wa
+    from chunk_windowed_softmax_gb300 import _build, inputs
+    _build.build()
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    info = plan.info()
+    pairs = info["kept_pairs"] * w.B * w.H
+    out, lse = plan.forward_lse(q, k, v)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    for _ in range(max(3, args.warmup)):
+        plan.backward(q, k, v, out, dout, lse, dq, dk, dv)
+    st = plan.check_error()
+    if st != 0:
+        raise SystemExit(f"device error during warm-up: {wa.wa_status_string(st)}")
+    sampler = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0])
+    time.sleep(0.3)
+    plan.profile(True)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        plan.backward(q, k, v, out, dout, lse, dq, dk, dv)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    ms = e0.elapsed_time(e1) / args.steps
+    kms, n = plan.profile_read_backward()
+    plan.profile(False)
+    clocks = sampler.stop(t0, t1)
+    st = plan.check_error()
+    plan.close()
+    if st != 0:
+        raise SystemExit(f"device error during the timed steps: {wa.wa_status_string(st)}")
+    kms = [x / max(1, n) for x in kms]
+    bf16_peak = peaks()[0]
+    useful = 10.0 * w.D * pairs
+    dq_tf = 6.0 * w.D * pairs / (kms[1] * 1e-3) / 1e12    # S, dP, dq products
+    dkdv_tf = 8.0 * w.D * pairs / (kms[2] * 1e-3) / 1e12  # S^T, dP^T, dv, dk products
+    print(json.dumps({
+        "metric": "backward kept-pair TFLOP/s (10 D flops per kept pair)", "value": useful / ms / 1e9,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, {"kept_pairs_per_head": info["kept_pairs"]}),
+        "kernels_ms": {"row_dots": kms[0], "dq": kms[1], "dk_dv": kms[2], "split_sums": kms[3]},
+        "kernel_tflops": {"dq": dq_tf, "dk_dv": dkdv_tf},
+        "kernel_frac_of_bf16_peak": {"dq": dq_tf / bf16_peak, "dk_dv": dkdv_tf / bf16_peak},
+        "gpu_launches": (3 + (1 if w.G > 0 else 0)) * args.steps, "clocks": clocks}), flush=True)
+
+
 def main():
     args = parse()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.backward:
+        run_backward(args, workload(args.workload))
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

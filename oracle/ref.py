@@ -227,3 +227,55 @@ def window_attention_backward(q, k, v, dout, T, S, K, r, G, global_pos):
             if G:
                 rows_backward(b, h, np.arange(g0, g0 + G), kept_set_of_global(T, S, G))
     return dq, dk, dv
+
+
+def window_attention_backward_rows(q, k, v, dout, T, S, K, r, G, global_pos, b, h, q_frames=(), global_q=False,
+                                   k_frames=()):
+    """The backward of one (b, h) slice restricted to some rows, for checking large workloads on a sample.
+
+    Returns (dq, dk, dv), three dicts {row index: float64 [D]}: dq for the rows of ``q_frames`` (and for the global
+    rows when ``global_q``), dk and dv for the rows of ``k_frames``. A query row's dq needs only its own kept set;
+    a key row's dk and dv need every query that keeps it. Those queries are found by testing each frame's kept set
+    (and every global query keeps every key), and each is handled as in ``window_attention_backward``; so every
+    returned row equals the matching row of that function.
+    """
+    D = q.shape[-1]
+    scale = 1.0 / math.sqrt(D)
+    f0, g0 = frame_offset(G, global_pos), global_offset(T, S, global_pos)
+    qs, ks, vs, ds = (_as64(x[b, :, h]) for x in (q, k, v, dout))
+    key_rows = np.concatenate([frame_rows(t, S, f0) for t in k_frames]) if k_frames else np.zeros(0, np.int64)
+    dq, dk, dv = {}, {}, {}
+    dk_acc = np.zeros((len(key_rows), D))
+    dv_acc = np.zeros((len(key_rows), D))
+
+    def block(rows, kept, want_dq):
+        _, p = attend(qs[rows], ks[kept], vs[kept], scale)
+        dp = ds[rows] @ vs[kept].T
+        dsc = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        if want_dq:
+            g = scale * (dsc @ ks[kept])
+            for i, row in enumerate(rows):
+                dq[int(row)] = g[i]
+        if len(key_rows):
+            pos = {int(x): i for i, x in enumerate(kept)}
+            cols = [pos.get(int(x), -1) for x in key_rows]
+            sel = np.array([c >= 0 for c in cols])
+            if sel.any():
+                c = np.array([x for x in cols if x >= 0])
+                dv_acc[sel] += p[:, c].T @ ds[rows]
+                dk_acc[sel] += scale * (dsc[:, c].T @ qs[rows])
+
+    for t in range(T):
+        kept = kept_set_of_frame(t, T, S, K, r, G, global_pos)
+        needed_for_keys = len(key_rows) > 0 and np.isin(key_rows, kept).any()
+        if t in q_frames or needed_for_keys:
+            block(frame_rows(t, S, f0), kept, t in q_frames)
+    if G and (global_q or len(key_rows)):
+        kept = kept_set_of_global(T, S, G)
+        rows = np.arange(g0, g0 + G, dtype=np.int64)
+        for lo in range(0, G, 256):  # bounded score blocks: G x L may not fit in memory at once
+            block(rows[lo:lo + 256], kept, global_q)
+    for i, row in enumerate(key_rows):
+        dk[int(row)] = dk_acc[i]
+        dv[int(row)] = dv_acc[i]
+    return dq, dk, dv

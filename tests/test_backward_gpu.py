@@ -162,3 +162,30 @@ def test_backward_watchdog(cuda, flag):
         plan.close()
     want = ref.window_attention_backward(q, k, v, dout, w.T, w.S, w.K, w.r, w.G, w.global_pos)
     check_grads(got, want, "after watchdog")
+
+
+def test_backward_h3_sampled(cuda):
+    """The full H3 layer (56 heads, L = 99,968) in the benchmark's launch configuration; the oracle checks one head
+    on a sample: dq of chunk 0, a middle chunk and all global rows; dk, dv of the keys of a middle chunk (each
+    needs every query that keeps it: three chunks of frames and all global queries)."""
+    w = configs.H3
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    got = gpu_backward(cuda, w, q, k, v, dout)
+    h = 27
+    qh, kh, vh, doh = (t[:, :, h:h + 1].cpu() for t in (q, k, v, dout))
+    gq, gk, gv = (t[0, :, h].float().cpu().double().numpy() for t in got)
+    del q, k, v, dout, got
+    mid = w.nc // 2
+    q_frames = ref.chunk_frames(0, w.T, w.K) + ref.chunk_frames(mid, w.T, w.K)
+    k_frames = ref.chunk_frames(mid, w.T, w.K)
+    rdq, rdk, rdv = ref.window_attention_backward_rows(qh, kh, vh, doh, w.T, w.S, w.K, w.r, w.G, w.global_pos, 0, 0,
+                                                       q_frames=q_frames, global_q=True, k_frames=k_frames)
+    for name, g, ref_rows in (("dq", gq, rdq), ("dk", gk, rdk), ("dv", gv, rdv)):
+        rows = sorted(ref_rows)
+        want = np.stack([ref_rows[r] for r in rows])
+        have = g[rows]
+        rel = np.linalg.norm(have - want) / np.linalg.norm(want)
+        ab = np.abs(have - want).max() / np.abs(want).max()
+        print(f"h3 {name} ({len(rows)} rows): rel {rel:.2e} abs {ab:.2e}")
+        assert rel <= GRAD_REL and ab <= GRAD_ABS, f"h3 {name}: rel {rel:.3e} abs {ab:.3e}"

@@ -132,3 +132,28 @@ def test_planted_backward_mistakes_are_caught(mistake):
     assert not all(np.allclose(g, w, atol=1e-6) for g, w in zip(got, want))
     clean = _backward_with_mistake(q, k, v, dout, *geo, None)
     assert all(np.allclose(g, w, atol=1e-6) for g, w in zip(clean, want))
+
+
+@pytest.mark.parametrize("geo", [(7, 3, 2, 1, 4, 0), (9, 2, 3, 1, 5, 1), (6, 4, 1, 0, 0, 0), (5, 3, 2, 3, 2, 1)])
+def test_backward_rows_equal_full_backward(geo):
+    """The row-restricted backward (used on samples of large workloads) returns exactly the rows of the full one."""
+    T, S, K, r, G, gp = geo
+    L = T * S + G
+    rng = np.random.default_rng(sum(geo) + 7)
+    q, k, v = rand_qkv(rng, 2, L, 2, 4)
+    dout = rng.standard_normal(q.shape)
+    full = ref.window_attention_backward(q, k, v, dout, *geo)
+    f0 = G if gp else 0
+    g0 = 0 if gp else T * S
+    for b, h in ((0, 1), (1, 0)):
+        q_frames, k_frames = (0, T // 2), (T - 1, T // 2)
+        dq, dk, dv = ref.window_attention_backward_rows(q, k, v, dout, *geo, b, h, q_frames=q_frames,
+                                                        global_q=G > 0, k_frames=k_frames)
+        q_rows = [f0 + t * S + i for t in q_frames for i in range(S)] + list(range(g0, g0 + G))
+        k_rows = [f0 + t * S + i for t in k_frames for i in range(S)]
+        assert sorted(dq) == sorted(set(q_rows)) and sorted(dk) == sorted(set(k_rows)) == sorted(dv)
+        for row in q_rows:
+            np.testing.assert_allclose(dq[row], full[0][b, row, h], rtol=1e-12, atol=1e-12)
+        for row in k_rows:
+            np.testing.assert_allclose(dk[row], full[1][b, row, h], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(dv[row], full[2][b, row, h], rtol=1e-12, atol=1e-12)
