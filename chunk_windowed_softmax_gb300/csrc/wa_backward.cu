@@ -31,7 +31,6 @@ using namespace ptx;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms: waiting for in-flight copies while unwinding
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kBwdThreads = 192;  // warps 0-3 elementwise, warp 4 MMA issuer, warp 5 loads
 
 struct BwdParams {
   const Item* items;
@@ -80,11 +79,12 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
   for (int hf = 0; hf < D / 64; ++hf) tma_load_4d(dst + hf * kTileRows * 128, map, bar, hf * 64, h, row, b);
 }
 
-// One accumulator row (fp32 in TMEM, D columns) times `mul`: bf16 into `dst`, or fp32 into `part` when that is set.
-template <int D>
-__device__ __forceinline__ void store_row(uint32_t t_acc, float mul, bool row_ok, __nv_bfloat16* dst, float* part) {
+// Columns [c_lo, c_lo + NC) of one accumulator row (fp32 in TMEM) times `mul`: bf16 into `dst`, or fp32 into `part`
+// when that is set (both already offset to column c_lo).
+template <int NC>
+__device__ __forceinline__ void store_cols(uint32_t t_acc, float mul, bool row_ok, __nv_bfloat16* dst, float* part) {
 #pragma unroll
-  for (int c0 = 0; c0 < D; c0 += 32) {
+  for (int c0 = 0; c0 < NC; c0 += 32) {
     uint32_t o[32];
     tmem_ld_x32(t_acc + c0, o);  // warp-collective: every lane loads, only rows that exist store
     if (!row_ok) continue;
@@ -128,15 +128,45 @@ __device__ __forceinline__ void teardown(uint32_t tmem, int warp) {
   }
 }
 
+// Elementwise warps and column groups. Warp w < 4 kCG works on TMEM lanes 32 (w % 4) .. +31 (one row of the tile
+// per thread) and on the 128 / kCG columns of column group w / 4; so kCG warps share each sub-partition and hide
+// one another's latency. A group packs its bf16 results (P, dS) into the first half of its own column range, so no
+// group overwrites columns another group has yet to read; the MMAs that take them from TMEM address each 16-column
+// block accordingly (tmem_a_block).
+constexpr int kCG = 2;
+constexpr int kCW = kTileRows / kCG;            // columns per group
+constexpr int kEwWarps = 4 * kCG;
+// Two MMA issuers on different sub-partitions: one issuing thread shares its sub-partition with busy elementwise
+// warps, and a tcgen05.mma stream issued from there falls well below the tensor core's rate (about 110 instead of
+// 64 cycles per 128x128x16 MMA, measured), so each kernel splits its products between two threads. Each TMEM
+// region is written and read by MMAs of one thread only, so their in-order execution covers every hazard.
+constexpr int kMmaWarpX = kEwWarps, kMmaWarpY = kEwWarps + 1, kLoadWarp = kEwWarps + 2;
+constexpr int kBwdThreads = 32 * (kEwWarps + 3);
+
+// TMEM column offset of the bf16 A-operand block kk (16 rows of the reduction dimension: 8 packed columns) inside a
+// 128-column region whose groups each packed their half.
+__host__ __device__ constexpr uint32_t tmem_a_block(int kk) {
+  return (uint32_t)((kk * 16) / kCW * kCW + (kk % (kCW / 16)) * 8);
+}
+
+// First column and count of a group's share of a D-column accumulator row in the epilogue (at least 32 columns).
+template <int D>
+struct EpiCols {
+  static constexpr int kCols = D / kCG >= 32 ? D / kCG : 32;
+};
+
 // =====================================================================================================================
 // dq kernel: query-major. Each work item's query tiles are processed one after the other ("sub-items"), each against
 // the item's key segments, one 128-key tile per step.
-//   warps 0-3  elementwise: one thread per query row (TMEM lane); P = 2^(s c' - lse'), dS = P (dP - Dvec) as bf16
-//   warp 4     MMA issuer (one thread): S = Q K^T, dP = dout V^T, dq += dS K
-//   warp 5     TMA producer (one thread): Q and dout tiles of the sub-item, rings of key and value tiles
-// TMEM: R0, R1 [0,256) score buffers (step n's S in R[n % 2]; dS overwrites its first 64 columns as bf16 and is
-// the A operand of dS.K straight from TMEM), R2 [256,384) dP, R3 [384, 384+D) the dq accumulator. The next step's
-// S and dP are issued before this step's dS.K, so the elementwise work of a step overlaps the tensor core's.
+//   warps 0 .. 4 kCG - 1  elementwise: P = 2^(s c' - lse'), dS = P (dP - Dvec) as bf16, one row and one column
+//                          group per thread
+//   warp 4 kCG            MMA issuer X (one thread): S = Q K^T and dq += dS K
+//   warp 4 kCG + 1        MMA issuer Y (one thread): dP = dout V^T
+//   warp 4 kCG + 2        TMA producer (one thread): Q and dout tiles of the sub-item, rings of key and value tiles
+// TMEM: R0, R1 [0,256) score buffers (step n's S in R[n % 2]; dS, packed bf16, overwrites the front of each group's
+// columns and is the A operand of dS.K straight from TMEM), R2 [256,384) dP, R3 [384, 384+D) the dq accumulator.
+// The next step's S and dP are issued before this step's dS.K, so the elementwise work of a step overlaps the
+// tensor core's.
 // =====================================================================================================================
 template <int D>
 struct DqCfg {
@@ -146,14 +176,39 @@ struct DqCfg {
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKSlots * kTileBytes;
   static constexpr int kBarOff = kVOff + kVSlots * kTileBytes;
-  // q_full, q_empty, s_full[2], p_full[2], dp_free, o_full, drain, then the rings' full / empty barriers
-  static constexpr int kNumBars = 9 + 2 * kKSlots + 2 * kVSlots;
+  // q_full, q_empty, s_full[2], p_full[2], dp_free, o_full, drain_x, drain_y, then the rings' full / empty barriers
+  static constexpr int kNumBars = 10 + 2 * kKSlots + 2 * kVSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack of the dynamic window
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
   static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);   // dS from TMEM, key tile MN-major
 };
+
+// dS = P (dP - Dvec) for one thread's kCW columns of one row, packed to bf16 over the front of those columns.
+// kMask: columns at or past `valid` (a segment's ragged last tile) get P = 0.
+template <bool kMask>
+__device__ __forceinline__ void dq_row_step(uint32_t tS, const uint32_t (&dpr)[kCW / 32][32], float c_log2,
+                                            float neg_lse2, float drow, int col0, int valid) {
+#pragma unroll
+  for (int ch = 0; ch < kCW / 32; ++ch) {
+    uint32_t sr[32], pk[16];
+    tmem_ld_x32(tS + 32 * ch, sr);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), c_log2, neg_lse2));
+      float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), c_log2, neg_lse2));
+      if (kMask) {
+        const int col = col0 + 32 * ch + 2 * c;
+        p0 = col < valid ? p0 : 0.f;
+        p1 = col + 1 < valid ? p1 : 0.f;
+      }
+      pk[c] = pack_bf16(p0 * (__uint_as_float(dpr[ch][2 * c]) - drow),
+                        p1 * (__uint_as_float(dpr[ch][2 * c + 1]) - drow));
+    }
+    tmem_st_x16(tS + 16 * ch, pk);
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -165,13 +220,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const Smem sm = align_smem(smem_raw);
   const uint32_t sQ = sm.base + C::kQOff, sDO = sm.base + C::kDOOff, sK = sm.base + C::kKOff, sV = sm.base + C::kVOff;
   const uint32_t bar = sm.base + C::kBarOff;
-  const uint32_t b_qfull = bar, b_qempty = bar + 8, b_dpfree = bar + 48, b_ofull = bar + 56, b_drain = bar + 64;
+  const uint32_t b_qfull = bar, b_qempty = bar + 8, b_dpfree = bar + 48, b_ofull = bar + 56, b_drain_x = bar + 64,
+                 b_drain_y = bar + 72;
   auto b_sfull = [&](uint32_t n) { return bar + 16 + 8 * (n & 1); };
   auto b_pfull = [&](uint32_t n) { return bar + 32 + 8 * (n & 1); };
-  auto b_kfull = [&](uint32_t s) { return bar + 8 * (9 + s); };
-  auto b_kempty = [&](uint32_t s) { return bar + 8 * (9 + C::kKSlots + s); };
-  auto b_vfull = [&](uint32_t s) { return bar + 8 * (9 + 2 * C::kKSlots + s); };
-  auto b_vempty = [&](uint32_t s) { return bar + 8 * (9 + 2 * C::kKSlots + C::kVSlots + s); };
+  auto b_kfull = [&](uint32_t s) { return bar + 8 * (10 + s); };
+  auto b_kempty = [&](uint32_t s) { return bar + 8 * (10 + C::kKSlots + s); };
+  auto b_vfull = [&](uint32_t s) { return bar + 8 * (10 + 2 * C::kKSlots + s); };
+  auto b_vempty = [&](uint32_t s) { return bar + 8 * (10 + 2 * C::kKSlots + C::kVSlots + s); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -179,14 +235,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (tid == 0) {
     mbar_init(b_qfull, 1);
-    mbar_init(b_qempty, 1);
+    mbar_init(b_qempty, 2);  // both issuers: the last S (reads Q) and the last dP (reads dout) of the sub-item
     for (uint32_t n = 0; n < 2; ++n) {
-      mbar_init(b_sfull(n), 1);
-      mbar_init(b_pfull(n), 4);  // one arrival per elementwise warp
+      mbar_init(b_sfull(n), 2);         // S from issuer X, dP from issuer Y
+      mbar_init(b_pfull(n), kEwWarps);  // one arrival per elementwise warp
     }
-    mbar_init(b_dpfree, 4);
+    mbar_init(b_dpfree, kEwWarps);
     mbar_init(b_ofull, 1);
-    mbar_init(b_drain, 1);
+    mbar_init(b_drain_x, 1);
+    mbar_init(b_drain_y, 1);
     for (int s = 0; s < C::kKSlots; ++s) {
       mbar_init(b_kfull(s), 1);
       mbar_init(b_kempty(s), 1);
@@ -208,7 +265,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const uint32_t tR2 = tmem + 256, tR3 = tmem + 384;
 
-  if (warp == 5) {
+  if (warp == kLoadWarp) {
     // ---------------------------------------------------------------------------------------- TMA producer
     if (lane == 0) {
       uint32_t k_n = 0, v_n = 0, q_n = 0;
@@ -255,10 +312,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (q_n) mbar_wait_drain(b_qfull, (q_n - 1) & 1, kDrainLimitNs);
       }
     }
-  } else if (warp == 4) {
-    // ------------------------------------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarpX || warp == kMmaWarpY) {
+    // ---------------------------------------------------------------------------------------- MMA issuers
+    // X: S(n) = Q K_n^T into R[n % 2] and dq += dS(n) K_n; in its order S(n+1) comes before dq(n) and S(n+2) after
+    //    it, so the score buffer dq(n) reads is rewritten only behind it.
+    // Y: dP(n) = dout V_n^T into R2, once the elementwise warps have read dP(n-1).
+    const bool is_x = warp == kMmaWarpX;
     if (lane == 0) {
-      uint32_t k_n = 0, v_n = 0, q_n = 0, dpf_n = 0, gs = 0;  // gs: steps of all earlier sub-items
+      uint32_t k_n = 0, v_n = 0, q_n = 0, gs = 0;  // gs: steps of all earlier sub-items
       bool ok = true;
       const uint64_t dq_ = sdesc_sw128(sQ, 16, 1024), ddo = sdesc_sw128(sDO, 16, 1024);
       const uint64_t dk_ = sdesc_sw128(sK, 16, 1024), dv_ = sdesc_sw128(sV, 16, 1024);
@@ -279,67 +340,73 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int t = 0; t < ntq && ok; ++t) {
           ok = mbar_wait(b_qfull, q_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           q_n++;
-          uint32_t kcur = k_n % C::kKSlots;
-          ok = ok && mbar_wait(b_kfull(kcur), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-          k_n++;
-          uint32_t vs = v_n % C::kVSlots;
-          ok = ok && mbar_wait(b_vfull(vs), (v_n / C::kVSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-          v_n++;
           if (!ok) break;
-          tc_fence_after();
-          issue_nt(tmem + 128 * (gs & 1), (uint32_t)dq_, (uint32_t)dk_ + ((kcur * C::kTileBytes) >> 4));
-          issue_nt(tR2, (uint32_t)ddo, (uint32_t)dv_ + ((vs * C::kTileBytes) >> 4));
-          mma_commit(b_sfull(gs));
-          mma_commit(b_vempty(vs));
-          if (nt == 1) mma_commit(b_qempty);
-          for (int j = 0; j < nt && ok; ++j) {
-            const uint32_t n = gs + j;
-            uint32_t knext = 0;
-            if (j + 1 < nt) {
-              knext = k_n % C::kKSlots;
-              ok = mbar_wait(b_kfull(knext), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-              k_n++;
+          if (is_x) {
+            uint32_t kcur = k_n % C::kKSlots;
+            ok = mbar_wait(b_kfull(kcur), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            k_n++;
+            if (!ok) break;
+            tc_fence_after();
+            issue_nt(tmem + 128 * (gs & 1), (uint32_t)dq_, (uint32_t)dk_ + ((kcur * C::kTileBytes) >> 4));
+            mma_commit(b_sfull(gs));
+            if (nt == 1) mma_commit(b_qempty);
+            for (int j = 0; j < nt && ok; ++j) {
+              const uint32_t n = gs + j;
+              uint32_t knext = 0;
+              if (j + 1 < nt) {
+                knext = k_n % C::kKSlots;
+                ok = mbar_wait(b_kfull(knext), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+                k_n++;
+                if (!ok) break;
+                tc_fence_after();
+                issue_nt(tmem + 128 * ((n + 1) & 1), (uint32_t)dq_, (uint32_t)dk_ + ((knext * C::kTileBytes) >> 4));
+                mma_commit(b_sfull(n + 1));
+                if (j + 1 == nt - 1) mma_commit(b_qempty);  // every S of the sub-item has been issued
+              }
+              ok = mbar_wait(b_pfull(n), (n >> 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS(n) ready
               if (!ok) break;
               tc_fence_after();
-              issue_nt(tmem + 128 * ((n + 1) & 1), (uint32_t)dq_, (uint32_t)dk_ + ((knext * C::kTileBytes) >> 4));
-              ok = mbar_wait(b_dpfree, dpf_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dP(n) read
-              dpf_n++;
-              vs = v_n % C::kVSlots;
-              ok = ok && mbar_wait(b_vfull(vs), (v_n / C::kVSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              // dq += dS(n) K_n: dS from TMEM (16 keys per MMA, from R[n % 2]), K_n MN-major
+              const uint32_t kb = (uint32_t)dk_mn + ((kcur * C::kTileBytes) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < kTileRows / 16; ++kk)
+                mma_ts(tR3, tmem + 128 * (n & 1) + tmem_a_block(kk), kb + ((kk * 2048) >> 4), hi, C::kIdescDQ,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(b_kempty(kcur));
+              kcur = knext;
+            }
+            if (!ok) break;
+            mma_commit(b_ofull);
+          } else {
+            for (int j = 0; j < nt && ok; ++j) {
+              const uint32_t n = gs + j;
+              if (n > 0) {  // the elementwise warps have read dP(n-1) out of R2
+                ok = mbar_wait(b_dpfree, (n - 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+                if (!ok) break;
+              }
+              const uint32_t vs = v_n % C::kVSlots;
+              ok = mbar_wait(b_vfull(vs), (v_n / C::kVSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
               v_n++;
               if (!ok) break;
               tc_fence_after();
               issue_nt(tR2, (uint32_t)ddo, (uint32_t)dv_ + ((vs * C::kTileBytes) >> 4));
-              mma_commit(b_sfull(n + 1));
+              mma_commit(b_sfull(n));
               mma_commit(b_vempty(vs));
-              if (j + 1 == nt - 1) mma_commit(b_qempty);  // every MMA that reads Q or dout has been issued
+              if (j == nt - 1) mma_commit(b_qempty);  // every dP of the sub-item has been issued
             }
-            ok = mbar_wait(b_pfull(n), (n >> 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS(n) in TMEM
-            if (!ok) break;
-            tc_fence_after();
-            // dq += dS(n) K_n: dS from TMEM (first 64 columns of R[n % 2], 16 keys per MMA), K_n MN-major
-            const uint32_t kb = (uint32_t)dk_mn + ((kcur * C::kTileBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kTileRows / 16; ++kk)
-              mma_ts(tR3, tmem + 128 * (n & 1) + kk * 8, kb + ((kk * 2048) >> 4), hi, C::kIdescDQ,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(b_kempty(kcur));
-            kcur = knext;
           }
-          if (!ok) break;
-          ok = mbar_wait(b_dpfree, dpf_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // the last step's dP
-          dpf_n++;
-          if (!ok) break;
-          mma_commit(b_ofull);
           gs += nt;
         }
       }
-      mma_commit(b_drain);
-      mbar_wait_drain(b_drain, 0, ok ? kWaitLimitNs : kDrainLimitNs);
+      const uint32_t drain = is_x ? b_drain_x : b_drain_y;
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0, ok ? kWaitLimitNs : kDrainLimitNs);
     }
-  } else {
+  } else if (warp < kEwWarps) {
     // ---------------------------------------------------------------------------------------- elementwise
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int r = 32 * (warp & 3) + lane;  // query row in the tile == TMEM lane
+    const int col0 = kCW * (warp >> 2);   // this thread's key columns [col0, col0 + kCW)
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     uint32_t o_n = 0, gs = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
@@ -348,9 +415,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
       const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
       for (int t = 0; t < ntq && ok; ++t) {
-        const int row = it.q_lo + t * kTileRows + tid;
+        const int row = it.q_lo + t * kTileRows + r;
         const bool in_seq = row < prm.L;
-        const float lse2 = in_seq ? __ldg(prm.lse + (int64_t)it.bh * prm.L + row) * kLog2e : 0.f;
+        const float neg_lse2 = in_seq ? -__ldg(prm.lse + (int64_t)it.bh * prm.L + row) * kLog2e : 0.f;
         const float drow = in_seq ? __ldg(prm.dvec + (int64_t)it.bh * prm.L + row) : 0.f;
         for (int j = 0; j < nt; ++j) {
           const uint32_t n = gs + j;
@@ -360,25 +427,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
-          uint32_t dpr[128];
-          tmem_ld_x128(tR2 + lane_base, dpr);
+          uint32_t dpr[kCW / 32][32];
+#pragma unroll
+          for (int ch = 0; ch < kCW / 32; ++ch) tmem_ld_x32(tR2 + lane_base + col0 + 32 * ch, dpr[ch]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(b_dpfree);
-          const uint32_t tS = tmem + lane_base + 128 * (n & 1);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t sr[32], pk[16];
-            tmem_ld_x32(tS + 32 * q4, sr);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int c0 = 32 * q4 + 2 * c;
-              const float p0 = c0 < valid ? ex2(fmaf(__uint_as_float(sr[2 * c]), prm.c_log2, -lse2)) : 0.f;
-              const float p1 = c0 + 1 < valid ? ex2(fmaf(__uint_as_float(sr[2 * c + 1]), prm.c_log2, -lse2)) : 0.f;
-              pk[c] = pack_bf16(p0 * (__uint_as_float(dpr[c0]) - drow), p1 * (__uint_as_float(dpr[c0 + 1]) - drow));
-            }
-            tmem_st_x16(tS + 16 * q4, pk);
-          }
+          const uint32_t tS = tmem + lane_base + 128 * (n & 1) + col0;
+          if (valid >= kTileRows)
+            dq_row_step<false>(tS, dpr, prm.c_log2, neg_lse2, drow, col0, valid);
+          else
+            dq_row_step<true>(tS, dpr, prm.c_log2, neg_lse2, drow, col0, valid);
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
@@ -390,14 +449,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         o_n++;
         if (!ok) break;
         tc_fence_after();
-        const bool row_ok = row < it.q_hi;
-        const int b = it.bh / prm.H, h = it.bh % prm.H;
-        if (it.split < 0) {
-          store_row<D>(tR3 + lane_base, prm.scale, row_ok,
-                       prm.dq + (int64_t)b * prm.sb + (int64_t)row * prm.sl + (int64_t)h * prm.sh, nullptr);
-        } else {
-          const int64_t slot = ((int64_t)it.bh * prm.G + (row - prm.g0)) * prm.n_splits + it.split;
-          store_row<D>(tR3 + lane_base, prm.scale, row_ok, nullptr, prm.ws_dq + slot * D);
+        constexpr int EC = EpiCols<D>::kCols;
+        const int c_lo = EC * (warp >> 2);
+        if (c_lo < D) {
+          const bool row_ok = row < it.q_hi;
+          const int b = it.bh / prm.H, h = it.bh % prm.H;
+          if (it.split < 0) {
+            store_cols<EC>(tR3 + lane_base + c_lo, prm.scale, row_ok,
+                           prm.dq + (int64_t)b * prm.sb + (int64_t)row * prm.sl + (int64_t)h * prm.sh + c_lo, nullptr);
+          } else {
+            const int64_t slot = ((int64_t)it.bh * prm.G + (row - prm.g0)) * prm.n_splits + it.split;
+            store_cols<EC>(tR3 + lane_base + c_lo, prm.scale, row_ok, nullptr, prm.ws_dq + slot * D + c_lo);
+          }
         }
         tc_fence_before();
         gs += nt;
@@ -410,15 +473,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // =====================================================================================================================
 // dk / dv kernel: key-major. Item rows are read as keys (one 128-key tile per sub-item, resident for the sub-item)
 // and the item's segments as the queries that keep them, streamed one 128-query tile per step.
-//   warps 0-3  elementwise: one thread per key (TMEM lane). Phase A: P^T = 2^(s c' - lse'_col) -> bf16 into TMEM.
-//              Phase B: dS^T = P^T (dP^T - Dvec_col) -> bf16 into TMEM. P stays in fp32 registers between them.
-//   warp 4     MMA issuer: S^T = K Q^T, dP^T = V dout^T, dv += P^T dout, dk += dS^T Q
-//   warp 5     loads (all lanes): lane 0 issues the TMA copies (the key / value tiles of the sub-item and a ring of
-//              query / dout tiles); every lane then stages 4 query columns' (lse, Dvec) into the ring slot.
-// TMEM: S^T [0,128) (P^T over its first 64 columns), dP^T [128,256) (dS^T over its first 64), dv [256, 256+D),
-// dk [384, 384+D). Issue order per step n: dv(n) after P^T(n) is written, then S^T(n+1); dk(n) after dS^T(n), then
-// dP^T(n+1). So the tensor core computes dv(n) and S^T(n+1) while the elementwise warps work on dS^T(n), and dk(n)
-// and dP^T(n+1) while they start P^T(n+1).
+//   warps 0 .. 4 kCG - 1  elementwise, one key (TMEM lane) and one group of query columns per thread.
+//                          Phase A: P^T = 2^(s c' - lse'_col) -> bf16 into TMEM. Phase B: dS^T = P^T (dP^T - Dvec_col)
+//                          -> bf16 into TMEM. P stays in fp32 registers between the phases.
+//   warp 4 kCG            MMA issuer: S^T = K Q^T, dP^T = V dout^T, dv += P^T dout, dk += dS^T Q
+//   warp 4 kCG + 1        idle (the dq kernel's second issuer; both kernels share one launch shape)
+//   warp 4 kCG + 2        loads (all lanes): lane 0 issues the TMA copies (the key / value tiles of the sub-item and
+//                          a ring of query / dout tiles); every lane then stages 4 query columns' values
+//                          (log2-domain lse, Dvec) into the ring slot. Columns past the segment get lse' = +inf and
+//                          Dvec = 0, so their P and dS are exactly 0 with no masking in the elementwise code.
+// TMEM: S^T [0,128) (P^T packed over the front of each group's columns), dP^T [128,256) (dS^T likewise),
+// dv [256, 256+D), dk [384, 384+D). Issue order per step n: dv(n) after P^T(n) is written, then S^T(n+1); dk(n)
+// after dS^T(n), then dP^T(n+1). So the tensor core computes dv(n) and S^T(n+1) while the elementwise warps work on
+// dS^T(n), and dk(n) and dP^T(n+1) while they start P^T(n+1).
 // =====================================================================================================================
 template <int D>
 struct DkvCfg {
@@ -427,10 +494,10 @@ struct DkvCfg {
   static constexpr int kSlotBytes = 2 * kTileBytes;
   static constexpr int kKOff = 0, kVOff = kTileBytes;
   static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kColOff = kRingOff + kQSlots * kSlotBytes;  // per slot: 64 x float4 {lse'_c, lse'_c+1, D_c, D_c+1}
+  static constexpr int kColOff = kRingOff + kQSlots * kSlotBytes;  // per slot: 64 x {lse'_c, lse'_c+1, D_c, D_c+1}
   static constexpr int kColBytes = 64 * 16;
   static constexpr int kBarOff = kColOff + kQSlots * kColBytes;
-  // kv_full, kv_empty, s_full, p_full, dp_full, ds_full, o_full, drain, then q_full[slots], q_empty[slots]
+  // kv_full, kv_empty, s_full, p_full, dp_full, ds_full, o_full, drain_x, then q_full[slots], q_empty[slots]
   static constexpr int kNumBars = 8 + 2 * kQSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
@@ -448,12 +515,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const Smem sm = align_smem(smem_raw);
   const uint32_t sK = sm.base + C::kKOff, sV = sm.base + C::kVOff, sRing = sm.base + C::kRingOff;
+  const uint32_t sCol = sm.base + C::kColOff;
   const uint32_t bar = sm.base + C::kBarOff;
   const uint32_t b_kvfull = bar, b_kvempty = bar + 8, b_sfull = bar + 16, b_pfull = bar + 24, b_dpfull = bar + 32,
-                 b_dsfull = bar + 40, b_ofull = bar + 48, b_drain = bar + 56;
+                 b_dsfull = bar + 40, b_ofull = bar + 48, b_drain_x = bar + 56;
   auto b_qfull = [&](uint32_t s) { return bar + 8 * (8 + s); };
   auto b_qempty = [&](uint32_t s) { return bar + 8 * (8 + C::kQSlots + s); };
-  float4* colbuf = reinterpret_cast<float4*>(sm.p + C::kColOff);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -463,14 +530,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(b_kvfull, 1);
     mbar_init(b_kvempty, 1);
     mbar_init(b_sfull, 1);
-    mbar_init(b_pfull, 4);
+    mbar_init(b_pfull, kEwWarps);
     mbar_init(b_dpfull, 1);
-    mbar_init(b_dsfull, 4);
+    mbar_init(b_dsfull, kEwWarps);
     mbar_init(b_ofull, 1);
-    mbar_init(b_drain, 1);
+    mbar_init(b_drain_x, 1);
     for (int s = 0; s < C::kQSlots; ++s) {
       mbar_init(b_qfull(s), 1 + 32);  // the copies' expect-tx arrival + one per loader lane (column values)
-      mbar_init(b_qempty(s), 1 + 4);  // the MMA commit + one per elementwise warp (column values read)
+      mbar_init(b_qempty(s), 1 + kEwWarps);  // the MMA commit after dk(j) + one per elementwise warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -485,7 +552,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
 
-  if (warp == 5) {
+  if (warp == kLoadWarp) {
     // ------------------------------------------------------------------------------------------- loaders
     uint32_t kv_n = 0, q_n = 0;
     bool ok = true, dropped = false;
@@ -515,7 +582,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int c = 4 * lane + i;
-            l4[i] = c < valid ? __ldg(lse_bh + row + c) * kLog2e : 0.f;
+            l4[i] = c < valid ? __ldg(lse_bh + row + c) * kLog2e : INFINITY;
             d4[i] = c < valid ? __ldg(dv_bh + row + c) : 0.f;
           }
           const uint32_t qs = q_n % C::kQSlots;
@@ -533,9 +600,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               load_tile<D>(dst + C::kTileBytes, &tm_do, b_qfull(qs), h, row, b);
             }
           }
-          float4* cb = colbuf + qs * 64 + 2 * lane;
-          cb[0] = make_float4(l4[0], l4[1], d4[0], d4[1]);
-          cb[1] = make_float4(l4[2], l4[3], d4[2], d4[3]);
+          const uint32_t cb = sCol + qs * C::kColBytes + 32 * lane;
+          sts_f4(cb, make_float4(l4[0], l4[1], d4[0], d4[1]));
+          sts_f4(cb + 16, make_float4(l4[2], l4[3], d4[2], d4[3]));
           mbar_arrive(b_qfull(qs));  // release: the column values are visible to whoever waits on q_full
           q_n++;
         }
@@ -546,8 +613,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (uint32_t n = q_n > (uint32_t)C::kQSlots ? q_n - C::kQSlots : 0; n < q_n; ++n)
         mbar_wait_drain(b_qfull(n % C::kQSlots), (n / C::kQSlots) & 1, kDrainLimitNs);
     }
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarpX) {
     // ------------------------------------------------------------------------------------------ MMA issuer
+    // One thread, in the order dv(j), S^T(j+1), dk(j), dP^T(j+1): the elementwise warps' next scores are queued
+    // right behind the product that frees their region. (A second issuer thread was measured slower here: the
+    // chain dv(j) -> S^T(j+1) -> phase A stays on one thread either way, and the other thread's products then
+    // compete with it on the tensor core.)
     if (lane == 0) {
       uint32_t kv_n = 0, q_n = 0, p_n = 0, ds_n = 0;
       bool ok = true;
@@ -566,7 +637,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_acc = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_ts(d_tmem, a_tmem + kk * 8, b_lo + ((kk * 2048) >> 4), hi, C::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(d_tmem, a_tmem + tmem_a_block(kk), b_lo + ((kk * 2048) >> 4), hi, C::kIdescAcc,
+                 (acc || kk > 0) ? 1u : 0u);
       };
       auto slot_k = [&](uint32_t s, uint32_t tile) { return (uint32_t)dr_k + ((s * C::kSlotBytes + tile) >> 4); };
       auto slot_mn = [&](uint32_t s, uint32_t tile) { return (uint32_t)dr_mn + ((s * C::kSlotBytes + tile) >> 4); };
@@ -620,23 +692,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(b_ofull);
         }
       }
-      mma_commit(b_drain);
-      mbar_wait_drain(b_drain, 0, ok ? kWaitLimitNs : kDrainLimitNs);
+      mma_commit(b_drain_x);
+      mbar_wait_drain(b_drain_x, 0, ok ? kWaitLimitNs : kDrainLimitNs);
     }
-  } else {
+  } else if (warp < kEwWarps) {
     // ---------------------------------------------------------------------------------------- elementwise
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int r = 32 * (warp & 3) + lane;  // key row in the tile == TMEM lane
+    const int col0 = kCW * (warp >> 2);   // this thread's query columns [col0, col0 + kCW)
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     uint32_t q_n = 0, s_n = 0, o_n = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
       const Item it = load_item(prm.items, idx);
       const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
-      const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
-      const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+      const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
       for (int t = 0; t < ntk && ok; ++t) {
         for (int j = 0; j < nt; ++j) {
-          int valid;
-          step_row(it, j, nt0, &valid);
           const uint32_t qs = q_n % C::kQSlots;
           ok = mbar_wait(b_qfull(qs), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           ok = ok && mbar_wait(b_sfull, s_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
@@ -644,22 +715,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           q_n++;
           if (!ok) break;
           tc_fence_after();
-          const float4* cb = colbuf + qs * 64;
-          // Phase A: P^T = 2^(s c' - lse'_col) over this key's 128 query columns (columns past the segment: 0)
-          float p[128];
+          const uint32_t cb = sCol + qs * C::kColBytes + col0 * 8;  // 16 bytes per column pair
+          // Phase A: P^T = 2^(s c' - lse'_col) over this thread's query columns
+          float p[kCW];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int ch = 0; ch < kCW / 32; ++ch) {
             uint32_t sr[32], pk[16];
-            tmem_ld_x32(tS + lane_base + 32 * q4, sr);
+            tmem_ld_x32(tS + lane_base + col0 + 32 * ch, sr);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const int c0 = 32 * q4 + 2 * c;
-              const float4 cv = cb[c0 >> 1];
-              p[c0] = c0 < valid ? ex2(fmaf(__uint_as_float(sr[2 * c]), prm.c_log2, -cv.x)) : 0.f;
-              p[c0 + 1] = c0 + 1 < valid ? ex2(fmaf(__uint_as_float(sr[2 * c + 1]), prm.c_log2, -cv.y)) : 0.f;
-              pk[c] = pack_bf16(p[c0], p[c0 + 1]);
+              const int i = 32 * ch + 2 * c;
+              const float4 cv = lds_f4(cb + (i >> 1) * 16);
+              p[i] = ex2(fmaf(__uint_as_float(sr[2 * c]), prm.c_log2, -cv.x));
+              p[i + 1] = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), prm.c_log2, -cv.y));
+              pk[c] = pack_bf16(p[i], p[i + 1]);
             }
-            tmem_st_x16(tS + lane_base + 16 * q4, pk);
+            tmem_st_x16(tS + lane_base + col0 + 16 * ch, pk);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -672,17 +743,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int ch = 0; ch < kCW / 32; ++ch) {
             uint32_t dr[32], pk[16];
-            tmem_ld_x32(tDP + lane_base + 32 * q4, dr);
+            tmem_ld_x32(tDP + lane_base + col0 + 32 * ch, dr);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const int c0 = 32 * q4 + 2 * c;
-              const float4 cv = cb[c0 >> 1];
-              pk[c] = pack_bf16(p[c0] * (__uint_as_float(dr[2 * c]) - cv.z),
-                                p[c0 + 1] * (__uint_as_float(dr[2 * c + 1]) - cv.w));
+              const int i = 32 * ch + 2 * c;
+              const float4 cv = lds_f4(cb + (i >> 1) * 16);
+              pk[c] = pack_bf16(p[i] * (__uint_as_float(dr[2 * c]) - cv.z),
+                                p[i + 1] * (__uint_as_float(dr[2 * c + 1]) - cv.w));
             }
-            tmem_st_x16(tDP + lane_base + 16 * q4, pk);
+            tmem_st_x16(tDP + lane_base + col0 + 16 * ch, pk);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -698,17 +769,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         o_n++;
         if (!ok) break;
         tc_fence_after();
-        const int key = it.q_lo + t * kTileRows + tid;
-        const bool row_ok = key < it.q_hi;
-        const int b = it.bh / prm.H, h = it.bh % prm.H;
-        if (it.split < 0) {
-          const int64_t off = (int64_t)b * prm.sb + (int64_t)key * prm.sl + (int64_t)h * prm.sh;
-          store_row<D>(tDV + lane_base, 1.f, row_ok, prm.dv + off, nullptr);
-          store_row<D>(tDK + lane_base, prm.scale, row_ok, prm.dk + off, nullptr);
-        } else {
-          const int64_t slot = (((int64_t)it.bh * prm.G + (key - prm.g0)) * prm.n_splits + it.split) * D;
-          store_row<D>(tDV + lane_base, 1.f, row_ok, nullptr, prm.ws_dv + slot);
-          store_row<D>(tDK + lane_base, prm.scale, row_ok, nullptr, prm.ws_dk + slot);
+        constexpr int EC = EpiCols<D>::kCols;
+        const int c_lo = EC * (warp >> 2);
+        if (c_lo < D) {
+          const int key = it.q_lo + t * kTileRows + r;
+          const bool row_ok = key < it.q_hi;
+          const int b = it.bh / prm.H, h = it.bh % prm.H;
+          if (it.split < 0) {
+            const int64_t off = (int64_t)b * prm.sb + (int64_t)key * prm.sl + (int64_t)h * prm.sh + c_lo;
+            store_cols<EC>(tDV + lane_base + c_lo, 1.f, row_ok, prm.dv + off, nullptr);
+            store_cols<EC>(tDK + lane_base + c_lo, prm.scale, row_ok, prm.dk + off, nullptr);
+          } else {
+            const int64_t slot = (((int64_t)it.bh * prm.G + (key - prm.g0)) * prm.n_splits + it.split) * D + c_lo;
+            store_cols<EC>(tDV + lane_base + c_lo, 1.f, row_ok, nullptr, prm.ws_dv + slot);
+            store_cols<EC>(tDK + lane_base + c_lo, prm.scale, row_ok, nullptr, prm.ws_dk + slot);
+          }
         }
         tc_fence_before();
       }

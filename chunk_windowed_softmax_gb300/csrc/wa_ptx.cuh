@@ -235,6 +235,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 16-byte shared-memory load / store by 32-bit shared address (explicitly ld.shared / st.shared).
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
 // TMEM loads (32 lanes x 32-bit, N columns; the wait is inside the same statement so that no use of the
 // destination registers can be scheduled before the data has arrived) and stores (wait with tmem_wait_st).
 __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
