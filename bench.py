@@ -26,6 +26,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "kept-pair TFLOP/s and ms/call (1×GB300), % of dense BF16 tensor peak"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "window_attention_kernel_h3.md")
+BWD_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "backward_kernels_h3.md")
 
 
 def parse():
@@ -77,21 +78,21 @@ def peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def stored_traffic():
-    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if the kernel source it
-    was taken on is the current one (else None)."""
+def stored_traffic(summary=None, source="wa_kernels.cu", key="dram bytes per full H3 launch"):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, if the kernel source it was taken on is the
+    current one (else None)."""
     import hashlib
     try:
-        src = open(os.path.join(ROOT, "chunk_windowed_softmax_gb300", "csrc", "wa_kernels.cu"), "rb").read()
+        src = open(os.path.join(ROOT, "chunk_windowed_softmax_gb300", "csrc", source), "rb").read()
         digest = hashlib.sha256(src).hexdigest()[:16]
         fields = {}
-        for line in open(PROFILE_SUMMARY):
+        for line in open(summary or PROFILE_SUMMARY):
             if line.startswith("- ") and ":" in line:
                 k, v = line[2:].split(":", 1)
                 fields[k.strip()] = v.strip().strip("`")
         if fields.get("kernel source sha256[:16]") != digest:
             return None
-        return float(fields["dram bytes per full H3 launch"])
+        return float(fields[key])
     except Exception:
         return None
 
@@ -316,6 +317,10 @@ def run_backward(args, w):
         "kernels_ms": {"row_dots": kms[0], "dq": kms[1], "dk_dv": kms[2], "split_sums": kms[3]},
         "kernel_tflops": {"dq": dq_tf, "dk_dv": dkdv_tf},
         "kernel_frac_of_bf16_peak": {"dq": dq_tf / bf16_peak, "dk_dv": dkdv_tf / bf16_peak},
+        "roofline": {"bound": "tensor", "achieved": dkdv_tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": dkdv_tf / bf16_peak, "kernel": f"wa_dkdv_kernel<{w.D}>", "kernel_ms": kms[2],
+                     "traffic": stored_traffic(BWD_PROFILE_SUMMARY, "wa_backward.cu", "dk/dv dram bytes per full H3 launch")
+                     if w.name == "h3" else None},
         "gpu_launches": (3 + (1 if w.G > 0 else 0)) * args.steps, "clocks": clocks}), flush=True)
 
 
@@ -444,7 +449,7 @@ def main():
                          f"{f / 1e12:.3f} kept TFLOP, {s:.1f} s); throughput of the sample"}
 
     if rank == 0:
-        traffic = stored_traffic()
+        traffic = stored_traffic() if w.name == "h3" else None
         res = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
