@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //    it, so the score buffer dq(n) reads is rewritten only behind it.
     // Y: dP(n) = dout V_n^T into R2, once the elementwise warps have read dP(n-1).
     const bool is_x = warp == kMmaWarpX;
-    if (lane == 0) {
+    {  // the whole warp runs the issue loop; one elected lane issues (issue model in wa_ptx.cuh)
       uint32_t k_n = 0, v_n = 0, q_n = 0, gs = 0;  // gs: steps of all earlier sub-items
       bool ok = true;
       const uint64_t dq_ = sdesc_sw128(sQ, 16, 1024), ddo = sdesc_sw128(sDO, 16, 1024);
@@ -338,12 +338,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
         const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
         for (int t = 0; t < ntq && ok; ++t) {
-          ok = mbar_wait(b_qfull, q_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = mbar_wait_warp(b_qfull, q_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           q_n++;
           if (!ok) break;
           if (is_x) {
             uint32_t kcur = k_n % C::kKSlots;
-            ok = mbar_wait(b_kfull(kcur), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            ok = mbar_wait_warp(b_kfull(kcur), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
             k_n++;
             if (!ok) break;
             tc_fence_after();
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               uint32_t knext = 0;
               if (j + 1 < nt) {
                 knext = k_n % C::kKSlots;
-                ok = mbar_wait(b_kfull(knext), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+                ok = mbar_wait_warp(b_kfull(knext), (k_n / C::kKSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
                 k_n++;
                 if (!ok) break;
                 tc_fence_after();
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_commit(b_sfull(n + 1));
                 if (j + 1 == nt - 1) mma_commit(b_qempty);  // every S of the sub-item has been issued
               }
-              ok = mbar_wait(b_pfull(n), (n >> 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS(n) ready
+              ok = mbar_wait_warp(b_pfull(n), (n >> 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS(n) ready
               if (!ok) break;
               tc_fence_after();
               // dq += dS(n) K_n: dS from TMEM (16 keys per MMA, from R[n % 2]), K_n MN-major
@@ -381,11 +381,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int j = 0; j < nt && ok; ++j) {
               const uint32_t n = gs + j;
               if (n > 0) {  // the elementwise warps have read dP(n-1) out of R2
-                ok = mbar_wait(b_dpfree, (n - 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+                ok = mbar_wait_warp(b_dpfree, (n - 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
                 if (!ok) break;
               }
               const uint32_t vs = v_n % C::kVSlots;
-              ok = mbar_wait(b_vfull(vs), (v_n / C::kVSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              ok = mbar_wait_warp(b_vfull(vs), (v_n / C::kVSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
               v_n++;
               if (!ok) break;
               tc_fence_after();
@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // right behind the product that frees their region. (A second issuer thread was measured slower here: the
     // chain dv(j) -> S^T(j+1) -> phase A stays on one thread either way, and the other thread's products then
     // compete with it on the tensor core.)
-    if (lane == 0) {
+    {  // the whole warp runs the issue loop; one elected lane issues (issue model in wa_ptx.cuh)
       uint32_t kv_n = 0, q_n = 0, p_n = 0, ds_n = 0;
       bool ok = true;
       const uint64_t dk_ = sdesc_sw128(sK, 16, 1024), dv_ = sdesc_sw128(sV, 16, 1024);
@@ -647,10 +647,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
         const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
         for (int t = 0; t < ntk && ok; ++t) {
-          ok = mbar_wait(b_kvfull, kv_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = mbar_wait_warp(b_kvfull, kv_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           kv_n++;
           uint32_t qs = q_n % C::kQSlots;
-          ok = ok && mbar_wait(b_qfull(qs), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = ok && mbar_wait_warp(b_qfull(qs), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           q_n++;
           if (!ok) break;
           tc_fence_after();
@@ -660,7 +660,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(b_dpfull);
           if (nt == 1) mma_commit(b_kvempty);
           for (int j = 0; j < nt && ok; ++j) {
-            ok = mbar_wait(b_pfull, p_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // P^T(j) in TMEM
+            ok = mbar_wait_warp(b_pfull, p_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // P^T(j) in TMEM
             p_n++;
             if (!ok) break;
             tc_fence_after();
@@ -668,14 +668,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t qn = 0;
             if (j + 1 < nt) {
               qn = q_n % C::kQSlots;
-              ok = mbar_wait(b_qfull(qn), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              ok = mbar_wait_warp(b_qfull(qn), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
               q_n++;
               if (!ok) break;
               tc_fence_after();
               issue_nt(tS, (uint32_t)dk_, slot_k(qn, 0));  // S^T(j+1)
               mma_commit(b_sfull);
             }
-            ok = mbar_wait(b_dsfull, ds_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS^T(j) in TMEM
+            ok = mbar_wait_warp(b_dsfull, ds_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS^T(j) in TMEM
             ds_n++;
             if (!ok) break;
             tc_fence_after();

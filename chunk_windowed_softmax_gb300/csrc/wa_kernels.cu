@@ -13,8 +13,8 @@
 //   warp 9      TMA producer (one thread): Q tiles and a ring of K / V tiles, 128-byte swizzled
 //   warps 10-11 idle
 // The launch gives every thread 168 registers (384 x 168 = 64512); setmaxnreg then moves them to where the work
-// is: the softmax warpgroups rise to 200 (a full 128-column score row stays in registers), the third warpgroup
-// drops to 104. 2 x 128 x 200 + 128 x 104 = 64512, the launch's total. Each role branch ends with its own copy of
+// is: the softmax warpgroups rise to 192 (a full 128-column score row stays in registers), the third warpgroup
+// drops to 120. 2 x 128 x 192 + 128 x 120 = 64512, the launch's total. Each role branch ends with its own copy of
 // the teardown, so that no code is shared by regions with different register counts.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [384, 384+D). P_t (bf16) overwrites the
 // first 64 columns of S_t and is the A operand of the P.V MMA, read straight from TMEM.
@@ -42,8 +42,8 @@ using namespace ptx;
 constexpr int kThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
-constexpr uint32_t kSoftmaxRegs = 200;
-constexpr uint32_t kControlRegs = 104;
+constexpr uint32_t kSoftmaxRegs = 192;
+constexpr uint32_t kControlRegs = 120;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split exceeds the launch");
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O only when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
@@ -283,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (see the issue model in wa_ptx.cuh); one elected lane issues the MMAs.
+    {
       uint32_t k_n = 0, v_n = 0;
       uint32_t q_n0 = 0, q_n1 = 0, p_n0 = 0, p_n1 = 0;
       bool ok = true;
@@ -322,10 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
         const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
         const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
-        ok = mbar_wait(bars.q_full(0), q_n0 & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        ok = mbar_wait_warp(bars.q_full(0), q_n0 & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
         q_n0++;
         if (ok && ntq > 1) {
-          ok = mbar_wait(bars.q_full(1), q_n1 & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = mbar_wait_warp(bars.q_full(1), q_n1 & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           q_n1++;
         }
         if (!ok) break;
@@ -336,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++k_n;
           const uint32_t vslot = v_n % C::kVSlots, vpar = (v_n / C::kVSlots) & 1;  // V_j, used at step j + 1
           ++v_n;
-          ok = mbar_wait(bars.k_full(kslot), kpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
-          if (ok && j > 0) ok = mbar_wait(bars.v_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = mbar_wait_warp(bars.k_full(kslot), kpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          if (ok && j > 0) ok = mbar_wait_warp(bars.v_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t >= ntq) break;
             if (j > 0) {
               uint32_t& pn = t ? p_n1 : p_n0;
-              ok = mbar_wait(bars.p_full(t), pn & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              ok = mbar_wait_warp(bars.p_full(t), pn & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
               pn++;
               if (!ok) break;
               tc_fence_after();
@@ -365,14 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           prev_vpar = vpar;
         }
         if (!ok) break;
-        ok = mbar_wait(bars.v_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        ok = mbar_wait_warp(bars.v_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= ntq) break;
           uint32_t& pn = t ? p_n1 : p_n0;
-          ok = mbar_wait(bars.p_full(t), pn & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = mbar_wait_warp(bars.p_full(t), pn & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           pn++;
           if (!ok) break;
           tc_fence_after();
