@@ -64,20 +64,23 @@ struct Cfg {
   // Separate K and V rings; the producer runs K one tile ahead of V (K is needed a step earlier than V).
   static constexpr int kKSlots = kF8 ? 5 : (D == 128 ? 3 : 4);
   static constexpr int kVSlots = kF8 ? 3 : (D == 128 ? 2 : 4);
+  // Step bundles: the copies of step j (K_j and V_{j-1}) complete on one barrier and are released by one commit.
+  // Bundle b reuses a K slot last read in bundle <= b - kKSlots and a V slot last read in bundle <= b - kVSlots,
+  // so the producer waits for bundle b - kLag's release, kLag = min(kKSlots, kVSlots) (also the barrier count).
+  static constexpr int kLag = kKSlots < kVSlots ? kKSlots : kVSlots;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kQTileBytes;
   static constexpr int kVOff = kKOff + kKSlots * kQTileBytes;
   static constexpr int kBarOff = kVOff + kVSlots * kVTileBytes;
-  // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain k_full[kKSlots] k_empty[kKSlots]
-  //           v_full[kVSlots] v_empty[kVSlots]
-  static constexpr int kNumBars = 11 + 2 * kKSlots + 2 * kVSlots;
+  // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain b_full[kLag] b_empty[kLag]
+  static constexpr int kNumBars = 11 + 2 * kLag;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t kTmemO = 256;
   static constexpr uint32_t kIdescS = kF8 ? idesc_e4m3_f32(128, 128)
                                          : idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);   // P from TMEM, V MN-major (D contiguous)
-  static_assert(kBarOff + (11 + 2 * kKSlots + 2 * kVSlots) * 8 + 16 + 1024 <= 232448, "shared memory budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct Params {
@@ -96,8 +99,8 @@ struct Params {
 };
 
 // Shared-memory barrier layout, relative to the barrier block: q_full[2] q_empty[2] s_full[2] p_full[2]
-// o_full[2] drain, then the K and V ring barriers. Addresses are computed, never indexed from a local array.
-template <int KS, int VS>
+// o_full[2] drain, then the step-bundle barriers. Addresses are computed, never indexed from a local array.
+template <int NB>
 struct BarAddr {
   uint32_t base;
   __device__ __forceinline__ uint32_t q_full(int t) const { return base + 8 * (0 + t); }
@@ -106,10 +109,9 @@ struct BarAddr {
   __device__ __forceinline__ uint32_t p_full(int t) const { return base + 8 * (6 + t); }
   __device__ __forceinline__ uint32_t o_full(int t) const { return base + 8 * (8 + t); }
   __device__ __forceinline__ uint32_t drain() const { return base + 8 * 10; }
-  __device__ __forceinline__ uint32_t k_full(uint32_t slot) const { return base + 8 * (11 + slot); }
-  __device__ __forceinline__ uint32_t k_empty(uint32_t slot) const { return base + 8 * (11 + KS + slot); }
-  __device__ __forceinline__ uint32_t v_full(uint32_t slot) const { return base + 8 * (11 + 2 * KS + slot); }
-  __device__ __forceinline__ uint32_t v_empty(uint32_t slot) const { return base + 8 * (11 + 2 * KS + VS + slot); }
+  // bundle b: full (copies landed) and empty (the MMAs reading it completed)
+  __device__ __forceinline__ uint32_t b_full(uint32_t b) const { return base + 8 * (11 + b % NB); }
+  __device__ __forceinline__ uint32_t b_empty(uint32_t b) const { return base + 8 * (11 + NB + b % NB); }
 };
 
 __device__ __forceinline__ Item load_item(const Item* items, int idx) {
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
-  const BarAddr<C::kKSlots, C::kVSlots> bars{bar0};
+  const BarAddr<C::kLag> bars{bar0};
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -173,13 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.o_full(t), 1);
     }
     mbar_init(bars.drain(), 1);
-    for (int s = 0; s < C::kKSlots; ++s) {
-      mbar_init(bars.k_full(s), 1);
-      mbar_init(bars.k_empty(s), 1);
-    }
-    for (int s = 0; s < C::kVSlots; ++s) {
-      mbar_init(bars.v_full(s), 1);
-      mbar_init(bars.v_empty(s), 1);
+    for (int s = 0; s < C::kLag; ++s) {
+      mbar_init(bars.b_full(s), 1);
+      mbar_init(bars.b_empty(s), 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -214,37 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kLoadWarp) {
     // ------------------------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t k_n = 0, v_n = 0;  // K / V tiles loaded so far (ring slot = n % slots, phase = n / slots)
+      uint32_t k_n = 0, v_n = 0, b_n = 0;  // K tiles, V tiles and step bundles loaded so far
       uint32_t q_n0 = 0, q_n1 = 0;
       bool dropped = false;
       bool ok = true;
-      // Load one 128-row key or value tile into the next slot of its ring.
-      auto load_kv = [&](bool is_v, int row, int h, int b) -> bool {
-        uint32_t& n = is_v ? v_n : k_n;
-        const uint32_t slots = is_v ? C::kVSlots : C::kKSlots;
-        const uint32_t slot = n % slots;
-        const uint32_t empty = is_v ? bars.v_empty(slot) : bars.k_empty(slot);
-        const uint32_t full = is_v ? bars.v_full(slot) : bars.k_full(slot);
-        if (!mbar_wait(empty, ((n / slots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs)) return false;
-        if ((prm.debug_flags & 1) && !dropped && blockIdx.x == 0) {
-          dropped = true;  // fault injection for the watchdog test: this tile is never loaded
-        } else {
-          if (is_v) {
-            mbar_arrive_expect_tx(full, C::kVTileBytes);
-#pragma unroll
-            for (int hf = 0; hf < C::kVBoxes; ++hf)
-              tma_load_4d(sV + slot * C::kVTileBytes + hf * C::kBoxBytes, &tmap_v, full, hf * 64, h, row, b);
-          } else {
-            mbar_arrive_expect_tx(full, C::kQTileBytes);
-#pragma unroll
-            for (int hf = 0; hf < C::kQKBoxes; ++hf)
-              tma_load_4d(sK + slot * C::kQTileBytes + hf * C::kBoxBytes, &tmap_k, full, hf * C::kQKBoxElems, h,
-                          row, b);
-          }
-        }
-        n++;
-        return true;
-      };
       for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
         const Item it = load_item(prm.items, idx);
         const int b = it.bh / prm.H, h = it.bh % prm.H;
@@ -265,18 +236,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
         const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
         auto row_of = [&](int j) { return j < nt0 ? it.s0_lo + j * kTileRows : it.s1_lo + (j - nt0) * kTileRows; };
-        ok = ok && load_kv(false, row_of(0), h, b);
-        for (int j = 0; j < nt && ok; ++j) {
-          if (j + 1 < nt) ok = load_kv(false, row_of(j + 1), h, b);  // K_{j+1} before V_j
-          ok = ok && load_kv(true, row_of(j), h, b);
+        // Bundle j of the item: K_j (j < nt, for S(j)) and V_{j-1} (j >= 1, for P(j-1).V).
+        for (int j = 0; j <= nt && ok; ++j) {
+          if (b_n >= (uint32_t)C::kLag) {
+            const uint32_t w = b_n - C::kLag;
+            ok = mbar_wait(bars.b_empty(w), (w / C::kLag) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            if (!ok) break;
+          }
+          const uint32_t full = bars.b_full(b_n);
+          mbar_arrive_expect_tx(full, (j < nt ? C::kQTileBytes : 0) + (j >= 1 ? C::kVTileBytes : 0));
+          if ((prm.debug_flags & 1) && !dropped && blockIdx.x == 0 && j < nt) {
+            dropped = true;  // fault injection for the watchdog test: this key tile is never loaded
+          } else if (j < nt) {
+            const uint32_t slot = k_n % C::kKSlots;
+#pragma unroll
+            for (int hf = 0; hf < C::kQKBoxes; ++hf)
+              tma_load_4d(sK + slot * C::kQTileBytes + hf * C::kBoxBytes, &tmap_k, full, hf * C::kQKBoxElems, h,
+                          row_of(j), b);
+          }
+          if (j >= 1) {
+            const uint32_t slot = v_n % C::kVSlots;
+#pragma unroll
+            for (int hf = 0; hf < C::kVBoxes; ++hf)
+              tma_load_4d(sV + slot * C::kVTileBytes + hf * C::kBoxBytes, &tmap_v, full, hf * 64, h, row_of(j - 1),
+                          b);
+          }
+          if (j < nt) k_n++;
+          if (j >= 1) v_n++;
+          b_n++;
         }
       }
       if (!ok) {
         // Unwinding: wait (briefly) for the copies still in flight so that none lands after the CTA exits.
-        for (uint32_t n = k_n > (uint32_t)C::kKSlots ? k_n - C::kKSlots : 0; n < k_n; ++n)
-          mbar_wait_drain(bars.k_full(n % C::kKSlots), (n / C::kKSlots) & 1, kDrainLimitNs);
-        for (uint32_t n = v_n > (uint32_t)C::kVSlots ? v_n - C::kVSlots : 0; n < v_n; ++n)
-          mbar_wait_drain(bars.v_full(n % C::kVSlots), (n / C::kVSlots) & 1, kDrainLimitNs);
+        for (uint32_t n = b_n > (uint32_t)C::kLag ? b_n - C::kLag : 0; n < b_n; ++n)
+          mbar_wait_drain(bars.b_full(n), (n / C::kLag) & 1, kDrainLimitNs);
         if (q_n0) mbar_wait_drain(bars.q_full(0), (q_n0 - 1) & 1, kDrainLimitNs);
         if (q_n1) mbar_wait_drain(bars.q_full(1), (q_n1 - 1) & 1, kDrainLimitNs);
       }
@@ -285,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------------------------- MMA issuer
     // The whole warp runs this loop (see the issue model in wa_ptx.cuh); one elected lane issues the MMAs.
     {
-      uint32_t k_n = 0, v_n = 0;
+      uint32_t k_n = 0, v_n = 0, b_n = 0;
       uint32_t q_n0 = 0, q_n1 = 0, p_n0 = 0, p_n1 = 0;
       bool ok = true;
       // Descriptors are built once; a shared-memory offset is added to the start-address field (address >> 4,
@@ -330,17 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_n1++;
         }
         if (!ok) break;
-        tc_fence_after();
-        uint32_t prev_vslot = 0, prev_vpar = 0;
-        for (int j = 0; j < nt; ++j) {
-          const uint32_t kslot = k_n % C::kKSlots, kpar = (k_n / C::kKSlots) & 1;
-          ++k_n;
-          const uint32_t vslot = v_n % C::kVSlots, vpar = (v_n / C::kVSlots) & 1;  // V_j, used at step j + 1
-          ++v_n;
-          ok = mbar_wait_warp(bars.k_full(kslot), kpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
-          if (ok && j > 0) ok = mbar_wait_warp(bars.v_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        // Step j: O_t += P_t(j-1) V_{j-1} (j >= 1), then S_t = Q_t K_j^T (j < nt), per tile; j = nt only drains.
+        for (int j = 0; j <= nt; ++j) {
+          ok = mbar_wait_warp(bars.b_full(b_n), (b_n / C::kLag) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
+          const uint32_t kslot = k_n % C::kKSlots, vslot = v_n % C::kVSlots;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t >= ntq) break;
@@ -350,38 +338,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               pn++;
               if (!ok) break;
               tc_fence_after();
-              issue_pv(t, prev_vslot, j > 1);  // O_t += P_t(j-1) V_{j-1}
+              issue_pv(t, vslot, j > 1);  // O_t += P_t(j-1) V_{j-1}
+              if (j == nt) mma_commit(bars.o_full(t));
             }
-            issue_s(t, kslot);  // S_t = Q_t K_j^T
-            mma_commit(bars.s_full(t));
+            if (j < nt) {
+              issue_s(t, kslot);  // S_t = Q_t K_j^T
+              mma_commit(bars.s_full(t));
+            }
           }
           if (!ok) break;
-          mma_commit(bars.k_empty(kslot));
-          if (j > 0) mma_commit(bars.v_empty(prev_vslot));
+          mma_commit(bars.b_empty(b_n));  // K_j and V_{j-1} are free once these MMAs complete
           if (j == nt - 1) {
             mma_commit(bars.q_empty(0));
             if (ntq > 1) mma_commit(bars.q_empty(1));
           }
-          prev_vslot = vslot;
-          prev_vpar = vpar;
+          if (j < nt) k_n++;
+          if (j >= 1) v_n++;
+          b_n++;
         }
-        if (!ok) break;
-        ok = mbar_wait_warp(bars.v_full(prev_vslot), prev_vpar, abort_flag, err, kErrTimeout, kWaitLimitNs);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= ntq) break;
-          uint32_t& pn = t ? p_n1 : p_n0;
-          ok = mbar_wait_warp(bars.p_full(t), pn & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-          pn++;
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, prev_vslot, nt > 1);
-          mma_commit(bars.o_full(t));
-        }
-        if (!ok) break;
-        mma_commit(bars.v_empty(prev_vslot));
       }
       // Every MMA and every completion arrive must have landed before the CTA tears down.
       mma_commit(bars.drain());
