@@ -189,3 +189,53 @@ def test_backward_h3_sampled(cuda):
         ab = np.abs(have - want).max() / np.abs(want).max()
         print(f"h3 {name} ({len(rows)} rows): rel {rel:.2e} abs {ab:.2e}")
         assert rel <= GRAD_REL and ab <= GRAD_ABS, f"h3 {name}: rel {rel:.3e} abs {ab:.3e}"
+
+
+@pytest.mark.parametrize("kind", ["bhld", "padded"])
+def test_backward_strided_layouts(cuda, kind):
+    """The plan's strides apply to every tensor of the backward: q, k, v, out, dout and the three gradients."""
+    from test_parity_gpu import relayout, strides_of
+    w = configs.Workload("bwd_strided", B=2, H=3, D=128, T=6, S=50, K=2, r=1, G=20, global_pos=1, seed=51)
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    qs, ks, vs, ds = (relayout(t, kind) for t in (q, k, v, dout))
+    plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos, strides=strides_of(qs))
+    try:
+        out, lse = plan.forward_lse(qs, ks, vs)
+        grads = plan.backward(qs, ks, vs, out, ds, lse)
+        assert plan.check_error() == 0
+        assert all(tuple(g.stride()) == tuple(qs.stride()) for g in grads)
+    finally:
+        plan.close()
+    want = ref.window_attention_backward(q, k, v, dout, w.T, w.S, w.K, w.r, w.G, w.global_pos)
+    check_grads(grads, want, f"strided {kind}")
+
+
+def test_backward_argument_errors(cuda):
+    """Synchronous argument checks: nothing is launched for a misaligned pointer or outputs that overlap inputs."""
+    w = configs.TINY
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    try:
+        out, lse = plan.forward_lse(q, k, v)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        s = torch.cuda.current_stream().cuda_stream
+        args = [q, k, v, out, dout, lse, dq, dk, dv]
+        ptrs = [t.data_ptr() for t in args]
+        bad = list(ptrs)
+        bad[0] += 2  # q misaligned
+        with pytest.raises(cuda.WAError):
+            cuda.wa_backward(plan.handle, *bad, s)
+        bad = list(ptrs)
+        bad[6] = ptrs[7]  # dq overlaps dk
+        with pytest.raises(cuda.WAError):
+            cuda.wa_backward(plan.handle, *bad, s)
+        bad = list(ptrs)
+        bad[8] = ptrs[0]  # dv overlaps q
+        with pytest.raises(cuda.WAError):
+            cuda.wa_backward(plan.handle, *bad, s)
+        cuda.wa_backward(plan.handle, *ptrs, s)  # the valid call still works
+        assert plan.check_error() == 0
+    finally:
+        plan.close()
