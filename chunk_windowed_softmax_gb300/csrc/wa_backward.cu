@@ -195,16 +195,19 @@ __device__ __forceinline__ void dq_row_step(uint32_t tS, const uint32_t (&dpr)[k
     uint32_t sr[32], pk[16];
     tmem_ld_x32(tS + 32 * ch, sr);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), c_log2, neg_lse2));
-      float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), c_log2, neg_lse2));
+    for (int c = 0; c < 16; ++c) {  // packed pairs: one f32x2 instruction per two columns
+      float x0, x1, t0, t1, d0, d1;
+      fma2(x0, x1, __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]), c_log2, c_log2, neg_lse2, neg_lse2);
+      float p0 = ex2(x0);
+      float p1 = ex2(x1);
       if (kMask) {
         const int col = col0 + 32 * ch + 2 * c;
         p0 = col < valid ? p0 : 0.f;
         p1 = col + 1 < valid ? p1 : 0.f;
       }
-      pk[c] = pack_bf16(p0 * (__uint_as_float(dpr[ch][2 * c]) - drow),
-                        p1 * (__uint_as_float(dpr[ch][2 * c + 1]) - drow));
+      add2(t0, t1, __uint_as_float(dpr[ch][2 * c]), __uint_as_float(dpr[ch][2 * c + 1]), -drow, -drow);
+      mul2(d0, d1, p0, p1, t0, t1);
+      pk[c] = pack_bf16(d0, d1);
     }
     tmem_st_x16(tS + 16 * ch, pk);
   }

@@ -247,6 +247,18 @@ __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n"
+      "  .reg .b64 ra, rb, rd;\n"
+      "  mov.b64 ra, {%2, %3};\n"
+      "  mov.b64 rb, {%4, %5};\n"
+      "  mul.rn.f32x2 rd, ra, rb;\n"
+      "  mov.b64 {%0, %1}, rd;\n"
+      "}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format code 0 in bits 7-9 and 10-12), both K-major,
 // fp32 accumulator (bits 4-5 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
