@@ -497,7 +497,7 @@ struct DkvCfg {
   static constexpr int kSlotBytes = 2 * kTileBytes;
   static constexpr int kKOff = 0, kVOff = kTileBytes;
   static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kColOff = kRingOff + kQSlots * kSlotBytes;  // per slot: 64 x {lse'_c, lse'_c+1, D_c, D_c+1}
+  static constexpr int kColOff = kRingOff + kQSlots * kSlotBytes;  // per slot: lse'[128] then Dvec[128], fp32
   static constexpr int kColBytes = 64 * 16;
   static constexpr int kBarOff = kColOff + kQSlots * kColBytes;
   // kv_full, kv_empty, s_full, p_full, dp_full, ds_full, o_full, drain_x, then q_full[slots], q_empty[slots]
@@ -603,9 +603,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               load_tile<D>(dst + C::kTileBytes, &tm_do, b_qfull(qs), h, row, b);
             }
           }
-          const uint32_t cb = sCol + qs * C::kColBytes + 32 * lane;
-          sts_f4(cb, make_float4(l4[0], l4[1], d4[0], d4[1]));
-          sts_f4(cb + 16, make_float4(l4[2], l4[3], d4[2], d4[3]));
+          const uint32_t cb = sCol + qs * C::kColBytes + 16 * lane;
+          sts_f4(cb, make_float4(l4[0], l4[1], l4[2], l4[3]));
+          sts_f4(cb + 512, make_float4(d4[0], d4[1], d4[2], d4[3]));
           mbar_arrive(b_qfull(qs));  // release: the column values are visible to whoever waits on q_full
           q_n++;
         }
@@ -718,7 +718,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           q_n++;
           if (!ok) break;
           tc_fence_after();
-          const uint32_t cb = sCol + qs * C::kColBytes + col0 * 8;  // 16 bytes per column pair
+          const uint32_t cb = sCol + qs * C::kColBytes + col0 * 4;  // lse' of this thread's first column
           // Phase A: P^T = 2^(s c' - lse'_col) over this thread's query columns
           float p[kCW];
 #pragma unroll
@@ -726,12 +726,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t sr[32], pk[16];
             tmem_ld_x32(tS + lane_base + col0 + 32 * ch, sr);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int i = 32 * ch + 2 * c;
-              const float4 cv = lds_f4(cb + (i >> 1) * 16);
-              p[i] = ex2(fmaf(__uint_as_float(sr[2 * c]), prm.c_log2, -cv.x));
-              p[i + 1] = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), prm.c_log2, -cv.y));
-              pk[c] = pack_bf16(p[i], p[i + 1]);
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 lv = lds_f4(cb + (32 * ch + 4 * c4) * 4);  // lse' of 4 columns
+              const int i = 32 * ch + 4 * c4;
+              p[i] = ex2(fmaf(__uint_as_float(sr[4 * c4]), prm.c_log2, -lv.x));
+              p[i + 1] = ex2(fmaf(__uint_as_float(sr[4 * c4 + 1]), prm.c_log2, -lv.y));
+              p[i + 2] = ex2(fmaf(__uint_as_float(sr[4 * c4 + 2]), prm.c_log2, -lv.z));
+              p[i + 3] = ex2(fmaf(__uint_as_float(sr[4 * c4 + 3]), prm.c_log2, -lv.w));
+              pk[2 * c4] = pack_bf16(p[i], p[i + 1]);
+              pk[2 * c4 + 1] = pack_bf16(p[i + 2], p[i + 3]);
             }
             tmem_st_x16(tS + lane_base + col0 + 16 * ch, pk);
           }
@@ -750,11 +753,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t dr[32], pk[16];
             tmem_ld_x32(tDP + lane_base + col0 + 32 * ch, dr);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int i = 32 * ch + 2 * c;
-              const float4 cv = lds_f4(cb + (i >> 1) * 16);
-              pk[c] = pack_bf16(p[i] * (__uint_as_float(dr[2 * c]) - cv.z),
-                                p[i + 1] * (__uint_as_float(dr[2 * c + 1]) - cv.w));
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 dv4 = lds_f4(cb + 512 + (32 * ch + 4 * c4) * 4);  // Dvec of 4 columns
+              const int i = 32 * ch + 4 * c4;
+              pk[2 * c4] = pack_bf16(p[i] * (__uint_as_float(dr[4 * c4]) - dv4.x),
+                                     p[i + 1] * (__uint_as_float(dr[4 * c4 + 1]) - dv4.y));
+              pk[2 * c4 + 1] = pack_bf16(p[i + 2] * (__uint_as_float(dr[4 * c4 + 2]) - dv4.z),
+                                         p[i + 3] * (__uint_as_float(dr[4 * c4 + 3]) - dv4.w));
             }
             tmem_st_x16(tDP + lane_base + col0 + 16 * ch, pk);
           }
