@@ -136,10 +136,10 @@ __device__ __forceinline__ void teardown(uint32_t tmem, int warp) {
 constexpr int kCG = 2;
 constexpr int kCW = kTileRows / kCG;            // columns per group
 constexpr int kEwWarps = 4 * kCG;
-// Two MMA issuers on different sub-partitions: one issuing thread shares its sub-partition with busy elementwise
-// warps, and a tcgen05.mma stream issued from there falls well below the tensor core's rate (about 110 instead of
-// 64 cycles per 128x128x16 MMA, measured), so each kernel splits its products between two threads. Each TMEM
-// region is written and read by MMAs of one thread only, so their in-order execution covers every hazard.
+// Two MMA-issuing warps on different sub-partitions (the dq kernel uses both): an issuing warp shares its
+// sub-partition with busy elementwise warps, which slows its stream of tcgen05.mma below the tensor core's rate, so
+// the dq kernel splits its products between two warps. Each TMEM region is written and read by MMAs of one warp
+// only, so their in-order execution covers every hazard.
 constexpr int kMmaWarpX = kEwWarps, kMmaWarpY = kEwWarps + 1, kLoadWarp = kEwWarps + 2;
 constexpr int kBwdThreads = 32 * (kEwWarps + 3);
 
@@ -160,8 +160,8 @@ struct EpiCols {
 // the item's key segments, one 128-key tile per step.
 //   warps 0 .. 4 kCG - 1  elementwise: P = 2^(s c' - lse'), dS = P (dP - Dvec) as bf16, one row and one column
 //                          group per thread
-//   warp 4 kCG            MMA issuer X (one thread): S = Q K^T and dq += dS K
-//   warp 4 kCG + 1        MMA issuer Y (one thread): dP = dout V^T
+//   warp 4 kCG            MMA issuer X (whole warp, one elected lane issues): S = Q K^T and dq += dS K
+//   warp 4 kCG + 1        MMA issuer Y (whole warp, one elected lane issues): dP = dout V^T
 //   warp 4 kCG + 2        TMA producer (one thread): Q and dout tiles of the sub-item, rings of key and value tiles
 // TMEM: R0, R1 [0,256) score buffers (step n's S in R[n % 2]; dS, packed bf16, overwrites the front of each group's
 // columns and is the A operand of dS.K straight from TMEM), R2 [256,384) dP, R3 [384, 384+D) the dq accumulator.

@@ -9,8 +9,10 @@
 // CTA roles (384 threads = 3 warpgroups, one CTA per SM):
 //   warps 0-3   softmax warpgroup of query tile 0: one thread per query row / TMEM lane
 //   warps 4-7   softmax warpgroup of query tile 1
-//   warp 8      MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V with tcgen05.mma, accumulators in TMEM
-//   warp 9      TMA producer (one thread): Q tiles and a ring of K / V tiles, 128-byte swizzled
+//   warp 8      MMA issuer: S_t = Q_t K^T and O_t += P_t V with tcgen05.mma, accumulators in TMEM; the whole warp
+//               runs the loop and one elect.sync-chosen lane issues (the issue model in wa_ptx.cuh)
+//   warp 9      TMA producer (one thread): Q tiles and rings of K / V tiles, 128-byte swizzled; each step's K_j and
+//               V_{j-1} complete on one bundle barrier
 //   warps 10-11 idle
 // The launch gives every thread 168 registers (384 x 168 = 64512); setmaxnreg then moves them to where the work
 // is: the softmax warpgroups rise to 192 (a full 128-column score row stays in registers), the third warpgroup
