@@ -19,7 +19,7 @@ STATUS = {0: "WA_OK", 1: "WA_ERR_INVALID", 2: "WA_ERR_UNSUPPORTED", 3: "WA_ERR_O
 EXPORTS = ("wa_plan_create", "wa_forward", "wa_plan_check_error", "wa_plan_info", "wa_plan_release",
            "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount",
            "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static", "wa_forward_fp8", "wa_forward_lse",
-           "wa_backward", "wa_plan_profile_read_backward")
+           "wa_backward", "wa_plan_profile_read_backward", "wa_forward_host")
 
 
 class WAError(RuntimeError):
@@ -65,6 +65,8 @@ def lib():
         L.wa_forward.restype = ctypes.c_int
         L.wa_forward_lse.argtypes = [P, P, P, P, P, P, P]
         L.wa_forward_lse.restype = ctypes.c_int
+        L.wa_forward_host.argtypes = [P] * 6
+        L.wa_forward_host.restype = ctypes.c_int
         L.wa_backward.argtypes = [P] * 11
         L.wa_backward.restype = ctypes.c_int
         L.wa_plan_profile_read_backward.argtypes = [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
@@ -211,6 +213,26 @@ class Plan:
         wa_forward(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), s.cuda_stream)
         return out
 
+    def forward_host(self, q, k, v, out=None, stream=None):
+        """out <- window attention of HOST (CPU) bf16 tensors with the plan's layout; the copies to and from the
+        device are pipelined with the computation over head groups (pinned tensors let them overlap). Returns the
+        host tensor `out` once it is complete."""
+        import torch
+        lay = self.layout
+        shape = (lay.B, self.L, lay.H, lay.D)
+        strides = (lay.stride_b, lay.stride_l, lay.stride_h, 1)
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            if t.dtype != torch.bfloat16 or t.is_cuda or tuple(t.shape) != shape or tuple(t.stride()) != strides:
+                raise ValueError(f"{name} must be a bf16 CPU tensor of shape {shape} with the plan's strides")
+        if out is None:
+            out = torch.empty_strided(shape, strides, dtype=torch.bfloat16, pin_memory=q.is_pinned())
+        s = torch.cuda.current_stream() if stream is None else stream
+        _check(lib().wa_forward_host(self.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                                     ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                     ctypes.c_void_p(s.cuda_stream)), "wa_forward_host")
+        s.synchronize()
+        return out
+
     def forward_lse(self, q, k, v, out=None, lse=None, stream=None):
         """(out, lse): the forward and each row's natural-log log-sum-exp (fp32 [B, H, L]) for the backward."""
         import torch
@@ -305,24 +327,15 @@ class Plan:
 def forward(q, k, v, T, S, K, r, G, global_pos=0, out=None):
     """One-shot call: out = window attention of q, k, v ([B, L, H, D] bf16 on a CUDA device).
 
-    CPU tensors are accepted too (end-to-end use): they are copied to the current CUDA device (from pinned memory
-    when they are pinned), the attention runs there, and the result is copied back into a CPU tensor.
+    CPU tensors are accepted too (end-to-end use): wa_forward_host copies them to the current CUDA device in head
+    groups, overlapping the copies with the computation (pinned tensors let the copies run asynchronously), and
+    writes the result into a CPU tensor.
     """
-    import torch
     B, L, H, D = q.shape
-    on_host = not q.is_cuda
-    if on_host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
-    else:
-        qd, kd, vd = q, k, v
-    plan = Plan(T, S, K, r, G, B, H, D, global_pos)
+    plan = Plan(T, S, K, r, G, B, H, D, global_pos, strides=tuple(q.stride()[:3]))
     try:
-        od = plan.forward(qd, kd, vd, out=None if on_host else out)
+        if not q.is_cuda:
+            return plan.forward_host(q, k, v, out=out)
+        return plan.forward(q, k, v, out=out)
     finally:
         plan.close()
-    if on_host:
-        res = out if out is not None else torch.empty(od.shape, dtype=od.dtype, pin_memory=q.is_pinned())
-        res.copy_(od, non_blocking=False)
-        return res
-    return od

@@ -60,6 +60,8 @@ struct LaunchArgs {
   float* lse = nullptr;    // optional [B][H][L] fp32 output: natural-log sum of exp of each row's scaled scores
   int qk_fp8 = 0;          // q and k are e4m3 (scores by kind::f8f6f4 MMAs); v and out stay bf16
   float qk_scale = 1.0f;   // dequantisation factor of the scores: q_scale * k_scale (1 for bf16 inputs)
+  int head_first = 0;      // the merge covers the heads [head_first, head_first + head_count) of every batch entry
+  int head_count = 0;      // (0: all heads)
 };
 
 // Encode the tensor maps and launch the attention kernel; returns a CUDA error code (0 on success).

@@ -503,10 +503,12 @@ template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                                                       __nv_bfloat16* __restrict__ out, int rows, int G, int H, int g0,
                                                       int P, int64_t sb, int64_t sl, int64_t sh, float* lse_out,
-                                                      int L) {
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+                                                      int L, int h0, int nh) {
+  // rows = B * nh * G global rows of the heads [h0, h0 + nh)
+  const int rr = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
+  if (rr >= rows) return;
+  const int r = ((rr / (nh * G)) * H + h0 + (rr / G) % nh) * G + rr % G;  // index over all B * H * G rows
   constexpr int kPer = D / 32;
   const float* lse = ws_lse + (int64_t)r * P;
   const float* o = ws_o + (int64_t)r * P * D;
@@ -617,16 +619,17 @@ int launch_combine(const LaunchArgs& a, void* stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Geometry& g = *a.geo;
   const wa_layout_t& l = g.layout;
-  const int rows = l.B * l.H * g.G;
+  const int nh = a.head_count > 0 ? a.head_count : l.H;
+  const int rows = l.B * nh * g.G;
   const int blocks = (rows + 7) / 8;
   if (l.D == 128)
     combine_kernel<128><<<blocks, 256, 0, s>>>(a.ws_o, a.ws_lse, reinterpret_cast<__nv_bfloat16*>(a.out), rows, g.G,
                                                l.H, (int)g.g0, a.n_splits, l.stride_b, l.stride_l, l.stride_h, a.lse,
-                                               (int)g.L);
+                                               (int)g.L, a.head_first, nh);
   else
     combine_kernel<64><<<blocks, 256, 0, s>>>(a.ws_o, a.ws_lse, reinterpret_cast<__nv_bfloat16*>(a.out), rows, g.G,
                                               l.H, (int)g.g0, a.n_splits, l.stride_b, l.stride_l, l.stride_h, a.lse,
-                                              (int)g.L);
+                                              (int)g.L, a.head_first, nh);
   return (int)cudaGetLastError();
 }
 

@@ -43,6 +43,13 @@ struct wa_plan {
   float* d_bws = nullptr;
   int bprof_n = 0;
   std::vector<cudaEvent_t> bprof_ev;
+  // Host-buffer forward (allocated by the first wa_forward_host): device copies of q, k, v and out with the plan's
+  // layout, the work list regrouped by head group, two copy streams and the events that chain them.
+  uint8_t* d_stage = nullptr;
+  wa::Item* d_items_hg = nullptr;
+  std::vector<int> hg_first, hg_item_off;  // head group g: heads [hg_first[g], hg_first[g+1]), items likewise
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  std::vector<cudaEvent_t> hg_ev;  // per group: copies in, compute done; then start, copies out done
 };
 
 namespace wa {
@@ -195,6 +202,11 @@ void free_plan(wa_plan* p) {
   if (p->d_items) cudaFree(p->d_items);
   if (p->d_ws) cudaFree(p->d_ws);
   if (p->d_bws) cudaFree(p->d_bws);
+  if (p->d_stage) cudaFree(p->d_stage);
+  if (p->d_items_hg) cudaFree(p->d_items_hg);
+  for (cudaEvent_t e : p->hg_ev) cudaEventDestroy(e);
+  if (p->s_in) cudaStreamDestroy(p->s_in);
+  if (p->s_out) cudaStreamDestroy(p->s_out);
   if (p->d_err) cudaFree(p->d_err);
   if (p->done) cudaEventDestroy(p->done);
   for (cudaEvent_t e : p->prof_ev) cudaEventDestroy(e);
@@ -518,6 +530,136 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
   }
   if (wa::launch_backward(a, (void*)s, plan->num_sms, ev) != 0) return WA_ERR_CUDA;
   if (cudaEventRecord(plan->done, s) != cudaSuccess) return WA_ERR_CUDA;
+  plan->last_stream = s;
+  plan->have_last = true;
+  return WA_OK;
+}
+
+namespace {
+
+// Lazily set up what wa_forward_host needs; called with plan->mu held.
+wa_status prepare_host_path(wa_plan_t* plan, size_t span_bytes) {
+  const wa::Geometry& g = plan->hp.geo;
+  const wa_layout_t& l = g.layout;
+  if (plan->d_stage) return WA_OK;
+  // Head groups: heads adjacent in memory (stride_h == D) and batch entries one sequence apart let a group's rows be
+  // copied as one strided 2-D block; otherwise the whole tensor is one group.
+  const bool groupable = l.stride_h == l.D && l.stride_b == g.L * l.stride_l;
+  const int n_groups = groupable ? std::min(l.H, 8) : 1;
+  plan->hg_first.assign(n_groups + 1, 0);
+  for (int i = 0; i <= n_groups; ++i) plan->hg_first[i] = (int)((int64_t)l.H * i / n_groups);
+  std::vector<wa::Item> regrouped;
+  regrouped.reserve(plan->hp.items.size());
+  plan->hg_item_off.assign(n_groups + 1, 0);
+  for (int gi = 0; gi < n_groups; ++gi) {  // keep the longest-first order inside each group
+    for (const wa::Item& it : plan->hp.items) {
+      const int h = it.bh % l.H;
+      if (h >= plan->hg_first[gi] && h < plan->hg_first[gi + 1]) regrouped.push_back(it);
+    }
+    plan->hg_item_off[gi + 1] = (int)regrouped.size();
+  }
+  cudaError_t e = dev_alloc(&plan->d_stage, 4 * span_bytes);
+  if (e == cudaSuccess) e = dev_alloc(&plan->d_items_hg, std::max<size_t>(1, regrouped.size()) * sizeof(wa::Item));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (plan->d_stage) cudaFree(plan->d_stage);
+    plan->d_stage = nullptr;
+    if (plan->d_items_hg) cudaFree(plan->d_items_hg);
+    plan->d_items_hg = nullptr;
+    return e == cudaErrorMemoryAllocation ? WA_ERR_OOM : WA_ERR_CUDA;
+  }
+  if (cudaMemcpy(plan->d_items_hg, regrouped.data(), regrouped.size() * sizeof(wa::Item), cudaMemcpyHostToDevice) !=
+          cudaSuccess ||
+      cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking) != cudaSuccess)
+    return WA_ERR_CUDA;
+  plan->hg_ev.resize(2 * n_groups + 2);
+  for (cudaEvent_t& ev : plan->hg_ev)
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return WA_ERR_CUDA;
+  return WA_OK;
+}
+
+}  // namespace
+
+wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out,
+                          wa_stream_t stream) {
+  if (!plan || !q || !k || !v || !out) return WA_ERR_INVALID;
+  const wa::Geometry& g = plan->hp.geo;
+  const wa_layout_t& l = g.layout;
+  const size_t elems = (size_t)((l.B - 1) * l.stride_b + (g.L - 1) * l.stride_l + (l.H - 1) * l.stride_h + l.D);
+  const size_t span = 2 * elems;
+  uintptr_t o = (uintptr_t)out;
+  if (ranges_overlap(o, span, (uintptr_t)q, span) || ranges_overlap(o, span, (uintptr_t)k, span) ||
+      ranges_overlap(o, span, (uintptr_t)v, span))
+    return WA_ERR_INVALID;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) {
+    cudaGetLastError();
+    return WA_ERR_INVALID;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  std::lock_guard<std::mutex> lk(plan->mu);
+  const size_t stage_span = (span + 255) / 256 * 256;
+  wa_status st = prepare_host_path(plan, stage_span);
+  if (st != WA_OK) return st;
+  if (plan->have_last && plan->last_stream != s) {
+    if (cudaStreamWaitEvent(s, plan->done, 0) != cudaSuccess) return WA_ERR_CUDA;
+  }
+  uint8_t* dq = plan->d_stage;
+  uint8_t* dk = dq + stage_span;
+  uint8_t* dv = dk + stage_span;
+  uint8_t* dout = dv + stage_span;
+  const int n_groups = (int)plan->hg_first.size() - 1;
+  cudaEvent_t* ev_in = &plan->hg_ev[0];
+  cudaEvent_t* ev_comp = &plan->hg_ev[n_groups];
+  cudaEvent_t ev_start = plan->hg_ev[2 * n_groups], ev_outdone = plan->hg_ev[2 * n_groups + 1];
+  // The copy streams start behind everything already queued on the caller's stream (earlier users of the staging).
+  if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(plan->s_in, ev_start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(plan->s_out, ev_start, 0) != cudaSuccess)
+    return WA_ERR_CUDA;
+  const size_t pitch = (size_t)l.stride_l * 2;
+  for (int gi = 0; gi < n_groups; ++gi) {
+    const int h0 = plan->hg_first[gi], nh = plan->hg_first[gi + 1] - h0;
+    const size_t off = (size_t)h0 * l.stride_h * 2;
+    // copies in: one strided block per tensor (B*L rows of nh*D elements), or the whole span for one group
+    const void* src[3] = {q, k, v};
+    uint8_t* dst[3] = {dq, dk, dv};
+    for (int x = 0; x < 3; ++x) {
+      cudaError_t e = n_groups > 1
+                          ? cudaMemcpy2DAsync(dst[x] + off, pitch, (const uint8_t*)src[x] + off, pitch,
+                                              (size_t)nh * l.D * 2, (size_t)l.B * g.L, cudaMemcpyHostToDevice,
+                                              plan->s_in)
+                          : cudaMemcpyAsync(dst[x], src[x], span, cudaMemcpyHostToDevice, plan->s_in);
+      if (e != cudaSuccess) return WA_ERR_CUDA;
+    }
+    if (cudaEventRecord(ev_in[gi], plan->s_in) != cudaSuccess || cudaStreamWaitEvent(s, ev_in[gi], 0) != cudaSuccess)
+      return WA_ERR_CUDA;
+    // this group's items and merge rows, on the caller's stream
+    wa::LaunchArgs a;
+    a.q = dq; a.k = dk; a.v = dv; a.out = dout;
+    a.items = plan->d_items_hg + plan->hg_item_off[gi];
+    a.n_items = plan->hg_item_off[gi + 1] - plan->hg_item_off[gi];
+    a.ws_o = plan->d_ws;
+    a.ws_lse = plan->d_ws ? plan->d_ws + plan->ws_o_elems : nullptr;
+    a.err = plan->d_err;
+    a.n_splits = plan->hp.n_splits;
+    a.debug_flags = 0;
+    a.geo = &g;
+    a.head_first = h0;
+    a.head_count = nh;
+    if (a.n_items > 0 && wa::launch_attention(a, (void*)s, plan->num_sms) != 0) return WA_ERR_CUDA;
+    if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
+    if (cudaEventRecord(ev_comp[gi], s) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_comp[gi], 0) != cudaSuccess)
+      return WA_ERR_CUDA;
+    cudaError_t e = n_groups > 1
+                        ? cudaMemcpy2DAsync((uint8_t*)out + off, pitch, dout + off, pitch, (size_t)nh * l.D * 2,
+                                            (size_t)l.B * g.L, cudaMemcpyDeviceToHost, plan->s_out)
+                        : cudaMemcpyAsync(out, dout, span, cudaMemcpyDeviceToHost, plan->s_out);
+    if (e != cudaSuccess) return WA_ERR_CUDA;
+  }
+  if (cudaEventRecord(ev_outdone, plan->s_out) != cudaSuccess || cudaStreamWaitEvent(s, ev_outdone, 0) != cudaSuccess ||
+      cudaEventRecord(plan->done, s) != cudaSuccess)
+    return WA_ERR_CUDA;
   plan->last_stream = s;
   plan->have_last = true;
   return WA_OK;

@@ -126,6 +126,22 @@ wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const 
                          float k_scale, wa_stream_t stream);
 
 /*
+ * wa_forward on HOST buffers: q, k, v are read from host memory and out is written to host memory (all bf16 with
+ * the plan's layout; page-locked memory lets the copies run asynchronously and overlap the computation). The
+ * library keeps device copies of the four tensors in the plan (allocated by the first call: 4 x the layout's span,
+ * kept until the plan is freed). When heads are adjacent in memory (stride_h == D) and batch entries are one
+ * sequence apart (stride_b == L * stride_l), the heads are processed in up to 8 groups: group i+1's inputs are
+ * copied in, group i is computed (on `stream`) and group i-1's rows are copied out at the same time, on two
+ * library-owned copy streams chained to `stream` by events; other layouts run as one group. Results are identical
+ * to wa_forward. The call is asynchronous: out is complete when `stream` reaches this point (e.g. after
+ * cudaStreamSynchronize); q, k, v and out must stay valid until then.
+ * Errors: WA_ERR_INVALID for null pointers or out overlapping an input; WA_ERR_OOM when the device copies cannot
+ * be allocated; WA_ERR_CUDA when a copy or launch fails. Device-side failures: see wa_plan_check_error().
+ */
+wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out,
+                          wa_stream_t stream);
+
+/*
  * Gradients of a scalar loss through the forward: given dout = d(loss)/d(out), writes
  *   dq = d(loss)/dq, dk = d(loss)/dk, dv = d(loss)/dv
  * for the same kept sets as wa_forward (VDN-Minimax-H3 window-attention article, section 一 for the kept sets and
