@@ -130,7 +130,7 @@ wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const 
  * the plan's layout; page-locked memory lets the copies run asynchronously and overlap the computation). The
  * library keeps device copies of the four tensors in the plan (allocated by the first call: 4 x the layout's span,
  * kept until the plan is freed). When heads are adjacent in memory (stride_h == D) and batch entries are one
- * sequence apart (stride_b == L * stride_l), the heads are processed in up to 8 groups: group i+1's inputs are
+ * sequence apart (stride_b == L * stride_l), the heads are processed in up to 6 groups: group i+1's inputs are
  * copied in, group i is computed (on `stream`) and group i-1's rows are copied out at the same time, on two
  * library-owned copy streams chained to `stream` by events; other layouts run as one group. Results are identical
  * to wa_forward. The call is asynchronous: out is complete when `stream` reaches this point (e.g. after
