@@ -23,9 +23,10 @@
 // The two query tiles ping-pong: while one warpgroup runs the softmax of its tile, the tensor core works on the
 // other tile's products.
 //
-// Softmax state is fp32 in registers: running max m (in log2 units of the scaled score) and row sum l. The max
-// is only raised when it grows by more than 2^8, so the O rescale in TMEM is rare; this is exact because the
-// final normalisation uses the same m. Every wait is bounded; on expiry the kernel latches an error in the plan's
+// Softmax state is fp32 in registers: a reference max m (in log2 units of the scaled score) and row sum l. Each
+// step exponentiates against m and checks only the step's row sum: the exact row max is taken (and m raised, O
+// and l rescaled) when that sum exceeds 2^16 or is not finite, i.e. at an item's first step (m starts at -inf) and
+// when the scores jump. This is exact because the final normalisation uses the same m. Every wait is bounded; on expiry the kernel latches an error in the plan's
 // error word and unwinds.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -47,7 +48,7 @@ constexpr int kLoadWarp = 9;
 constexpr uint32_t kSoftmaxRegs = 192;
 constexpr uint32_t kControlRegs = 120;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split exceeds the launch");
-constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kLazyLimit = 65536.0f;  // a step's row sum above this (relative to the reference m) raises m
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms: waiting for in-flight copies while unwinding
 
@@ -399,42 +400,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= valid) s[c] = -INFINITY;
         }
-        // Row max: 8 independent chains of three-input maxima over 16 columns each.
-        float mx[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-          mx[a] = fmaxf(s[16 * a], s[16 * a + 15]);
-#pragma unroll
-          for (int c = 1; c < 15; c += 2) mx[a] = max3(mx[a], s[16 * a + c], s[16 * a + c + 1]);
-        }
-        const float m_cand =
-            fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7])) * prm.c_scale;
-        // The running max only moves when it grows by more than 2^8; the O rescale that a move needs is done
-        // after P is written (it does not need the scores, so the score row is dead by then).
-        float alpha = 1.f;
-        bool rescale = false;
-        if (j == 0) {
-          m = m_cand;
-        } else {
-          const bool need = m_cand > m + kRescaleThreshold;
-          rescale = __any_sync(0xffffffffu, need);
+        // P = 2^(s*c - m) against the current reference m, and its row sum. The reference only has to keep P finite
+        // and within a sane range, not equal the row max: the final normalisation divides by l built against the
+        // same reference. So the exact row max is computed only when this step's sum exceeds 2^16 (or is not
+        // finite; the first step of an item starts from m = -inf): then the warp takes the max, raises m, redoes
+        // the exponentials and rescales l and, after the first step, O.
+        float row_sum = exp_store_row(s, prm.c_scale, -m, tS);
+        const bool need = !(row_sum <= kLazyLimit);
+        if (__any_sync(0xffffffffu, need)) {  // warp-uniform: tcgen05.ld/st are warp-collective
+          float alpha = 1.f;
           if (need) {
-            alpha = ex2(m - m_cand);
+            // Row max: 8 independent chains of three-input maxima over 16 columns each.
+            float mx[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+              mx[a] = fmaxf(s[16 * a], s[16 * a + 15]);
+#pragma unroll
+              for (int c = 1; c < 15; c += 2) mx[a] = max3(mx[a], s[16 * a + c], s[16 * a + c + 1]);
+            }
+            const float m_cand =
+                fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7])) * prm.c_scale;
+            alpha = j == 0 ? 0.f : ex2(m - m_cand);
             m = m_cand;
           }
-        }
-        // P = 2^(s*c - m) in bf16 over S, and its row sum.
-        const float row_sum = exp_store_row(s, prm.c_scale, -m, tS);
-        l = l * alpha + row_sum;
-        if (rescale) {  // warp-uniform: tcgen05.ld/st are warp-collective
+          row_sum = exp_store_row(s, prm.c_scale, -m, tS);  // the same P again for the lanes that kept m
+          l = l * alpha + row_sum;
+          if (j > 0) {  // O holds earlier steps' sums only after the first step
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_x32(tO + c0, o);
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld_x32(tO + c0, o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st_x32(tO + c0, o);
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              tmem_st_x32(tO + c0, o);
+            }
           }
+        } else {
+          l += row_sum;
         }
         tmem_wait_st();
         tc_fence_before();
