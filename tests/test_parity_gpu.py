@@ -85,6 +85,10 @@ EDGE = [
     configs.Workload("single_row", B=1, H=1, D=128, T=1, S=1, K=1, r=0, G=0, global_pos=0, seed=19),
     configs.Workload("sharp_globals", B=1, H=2, D=128, T=12, S=64, K=3, r=1, G=256, global_pos=0, seed=20,
                      k_global_scale=4.0),
+    # the global keys (the last key segment) scaled x16: the scores jump so far that the exponentials against the
+    # frames' reference max overflow, and the softmax must raise its reference in the middle of an item
+    configs.Workload("score_jump", B=1, H=2, D=64, T=10, S=64, K=2, r=2, G=128, global_pos=0, seed=22,
+                     k_global_scale=16.0),
 ]
 
 
