@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "wa_device.cuh"
 #include "wa_internal.h"
 #include "wa_ptx.cuh"
 
@@ -28,8 +29,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
-constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms: waiting for in-flight copies while unwinding
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
@@ -51,25 +50,12 @@ struct BwdParams {
   int debug_flags;
 };
 
-__device__ __forceinline__ Item load_item(const Item* items, int idx) {
-  const int4* p = reinterpret_cast<const int4*>(items + idx);
-  int4 a = __ldg(p), b = __ldg(p + 1);
-  return Item{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-}
-
-__device__ __forceinline__ int seg_tiles(int lo, int hi) { return hi > lo ? (hi - lo + kTileRows - 1) / kTileRows : 0; }
-
 // First row of the j-th 128-row tile of an item's segments, and how many of its rows belong to the segment.
 __device__ __forceinline__ int step_row(const Item& it, int j, int nt0, int* valid) {
   const int lo = j < nt0 ? it.s0_lo + j * kTileRows : it.s1_lo + (j - nt0) * kTileRows;
   const int hi = j < nt0 ? it.s0_hi : it.s1_hi;
   *valid = min(kTileRows, hi - lo);
   return lo;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v2 = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v2);
 }
 
 // One 128-row tile of a [B, L, H, D] bf16 tensor: D / 64 boxes of 128 rows x 128 bytes (128-byte swizzle).

@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "wa_device.cuh"
 #include "wa_internal.h"
 #include "wa_ptx.cuh"
 
@@ -49,8 +50,6 @@ constexpr uint32_t kSoftmaxRegs = 192;
 constexpr uint32_t kControlRegs = 120;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split exceeds the launch");
 constexpr float kLazyLimit = 65536.0f;  // a step's row sum above this (relative to the reference m) raises m
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
-constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms: waiting for in-flight copies while unwinding
 
 // kF8: q and k are e4m3 (one byte per element) and the scores use kind::f8f6f4 MMAs; v, P and O stay bf16 / fp32.
 template <int D, bool kF8>
@@ -117,14 +116,6 @@ struct BarAddr {
   __device__ __forceinline__ uint32_t b_empty(uint32_t b) const { return base + 8 * (11 + NB + b % NB); }
 };
 
-__device__ __forceinline__ Item load_item(const Item* items, int idx) {
-  const int4* p = reinterpret_cast<const int4*>(items + idx);
-  int4 a = __ldg(p), b = __ldg(p + 1);
-  return Item{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-}
-
-__device__ __forceinline__ int seg_tiles(int lo, int hi) { return hi > lo ? (hi - lo + kTileRows - 1) / kTileRows : 0; }
-
 // Exponentiate one 128-column score row into bf16 P (written to TMEM over the row's S columns, 16 columns per
 // store) and return the fp32 row sum.
 __device__ __forceinline__ float exp_store_row(const float (&s)[128], float c_scale, float neg_m, uint32_t tS) {
@@ -139,8 +130,7 @@ __device__ __forceinline__ float exp_store_row(const float (&s)[128], float c_sc
       const float p0 = ex2(x0);
       const float p1 = ex2(x1);
       add2(sum[2 * (c & 3)], sum[2 * (c & 3) + 1], sum[2 * (c & 3)], sum[2 * (c & 3) + 1], p0, p1);
-      __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
-      pk[c] = *reinterpret_cast<uint32_t*>(&v2);
+      pk[c] = pack_bf16(p0, p1);
     }
     tmem_st_x16(tS + 16 * q4, pk);
   }
@@ -462,11 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_x32(tO + c0, o);
           uint32_t w[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(o[2 * c]) * inv_l,
-                                                      __uint_as_float(o[2 * c + 1]) * inv_l);
-            w[c] = *reinterpret_cast<uint32_t*>(&v2);
-          }
+          for (int c = 0; c < 16; ++c)
+            w[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
           if (row_ok) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
