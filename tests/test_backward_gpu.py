@@ -239,3 +239,12 @@ def test_backward_argument_errors(cuda):
         assert plan.check_error() == 0
     finally:
         plan.close()
+
+
+@pytest.mark.parametrize("w", __import__("test_parity_gpu").random_geometries(12, seed=8), ids=lambda w: w.name)
+def test_backward_random_geometries(cuda, w):
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    dout = inputs.make_dout(w, device="cuda")
+    got = gpu_backward(cuda, w, q, k, v, dout)
+    want = ref.window_attention_backward(q, k, v, dout, w.T, w.S, w.K, w.r, w.G, w.global_pos)
+    check_grads(got, want, w.name)

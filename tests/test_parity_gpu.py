@@ -187,3 +187,24 @@ def test_public_forward_host_buffers(cuda):
     want = ref.window_attention(q, k, v, w.T, w.S, w.K, w.r, w.G, w.global_pos)
     check_slices({(0, h): out[0, :, h].float().numpy() for h in range(w.H)},
                  {(0, h): want[0, :, h] for h in range(w.H)}, "host")
+
+
+def random_geometries(n, seed):
+    """Small seeded random geometries: ragged chunks, both global placements, D in {64, 128}, r up to past nc."""
+    import random
+    rnd = random.Random(seed)
+    out = []
+    for i in range(n):
+        T = rnd.randint(1, 14)
+        K = rnd.randint(1, 5)
+        nc = -(-T // K)
+        out.append(configs.Workload(f"rand{i}", B=rnd.randint(1, 2), H=rnd.randint(1, 3), D=rnd.choice([64, 128]),
+                                    T=T, S=rnd.randint(1, 97), K=K, r=rnd.randint(0, nc + 1),
+                                    G=rnd.choice([0, 1, rnd.randint(2, 300)]), global_pos=rnd.randint(0, 1),
+                                    seed=3000 + i))
+    return out
+
+
+@pytest.mark.parametrize("w", random_geometries(24, seed=7), ids=lambda w: w.name)
+def test_random_geometries(cuda, w):
+    full_compare(cuda, w)
