@@ -78,6 +78,16 @@ def peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def profile_fields(path):
+    """The `- key: value` lines of an ncu summary under profiles/ as a dict (values without backquotes)."""
+    fields = {}
+    for line in open(path):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].rsplit(":", 1)  # the last colon: keys may contain one ("sha256[:16]")
+            fields[k.strip()] = v.strip().strip("`")
+    return fields
+
+
 def stored_traffic(summary=None, source="wa_kernels.cu", key="dram bytes per full H3 launch"):
     """DRAM bytes per launch of a kernel from a committed ncu summary, if the kernel source it was taken on is the
     current one (else None)."""
@@ -85,11 +95,7 @@ def stored_traffic(summary=None, source="wa_kernels.cu", key="dram bytes per ful
     try:
         src = open(os.path.join(ROOT, "chunk_windowed_softmax_gb300", "csrc", source), "rb").read()
         digest = hashlib.sha256(src).hexdigest()[:16]
-        fields = {}
-        for line in open(summary or PROFILE_SUMMARY):
-            if line.startswith("- ") and ":" in line:
-                k, v = line[2:].split(":", 1)
-                fields[k.strip()] = v.strip().strip("`")
+        fields = profile_fields(summary or PROFILE_SUMMARY)
         if fields.get("kernel source sha256[:16]") != digest:
             return None
         return float(fields[key])

@@ -126,3 +126,17 @@ def test_radius_beyond_chunks_is_one_group(walib):
     info, groups, _ = describe(walib, 10, 7, 3, 5, 4, 0)
     assert info["n_groups"] == 1
     assert (groups[0]["q_lo"], groups[0]["q_hi"]) == (0, 70)
+
+
+def test_profile_summaries_parse():
+    """bench.py reads the kernel-source hash and the DRAM traffic from the committed ncu summaries."""
+    import os
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import bench
+    for path, key in ((bench.PROFILE_SUMMARY, "dram bytes per full H3 launch"),
+                      (bench.BWD_PROFILE_SUMMARY, "dk/dv dram bytes per full H3 launch")):
+        fields = bench.profile_fields(path)
+        assert len(fields["kernel source sha256[:16]"]) == 16
+        assert float(fields[key]) > 1e9
