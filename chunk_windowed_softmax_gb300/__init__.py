@@ -215,8 +215,8 @@ class Plan:
 
     def forward_host(self, q, k, v, out=None, stream=None):
         """out <- window attention of HOST (CPU) bf16 tensors with the plan's layout; the copies to and from the
-        device are pipelined with the computation over head groups (pinned tensors let them overlap). Returns the
-        host tensor `out` once it is complete."""
+        device are pipelined with the computation over pieces of the sequence (pinned tensors let them overlap).
+        Returns the host tensor `out` once it is complete."""
         import torch
         lay = self.layout
         shape = (lay.B, self.L, lay.H, lay.D)

@@ -44,12 +44,17 @@ struct wa_plan {
   int bprof_n = 0;
   std::vector<cudaEvent_t> bprof_ev;
   // Host-buffer forward (allocated by the first wa_forward_host): device copies of q, k, v and out with the plan's
-  // layout, the work list regrouped by head group, two copy streams and the events that chain them.
+  // layout, and the sequence cut into row pieces that are copied in one after the other. After piece p has arrived,
+  // launch p runs the work items whose rows have all arrived (their list regrouped by launch), and the frame rows of
+  // out that launch p completes are copied back while later pieces are still on their way.
   uint8_t* d_stage = nullptr;
-  wa::Item* d_items_hg = nullptr;
-  std::vector<int> hg_first, hg_item_off;  // head group g: heads [hg_first[g], hg_first[g+1]), items likewise
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  std::vector<cudaEvent_t> hg_ev;  // per group: copies in, compute done; then start, copies out done
+  wa::Item* d_items_pc = nullptr;
+  bool pc_rows = false;                          // pieces are row blocks (else one piece: the whole tensors)
+  std::vector<int64_t> pc_lo, pc_hi;             // piece p: sequence rows [pc_lo[p], pc_hi[p]) of every batch entry
+  std::vector<int> pc_item_off;                  // launch p: items [pc_item_off[p], pc_item_off[p + 1])
+  std::vector<std::vector<std::pair<int64_t, int64_t>>> pc_out;  // out row ranges complete after launch p
+  cudaStream_t s_in = nullptr, s_out = nullptr, s_c2 = nullptr;
+  std::vector<cudaEvent_t> pc_ev;                // per piece: copies in, launch done; then four for the whole call
 };
 
 namespace wa {
@@ -203,10 +208,11 @@ void free_plan(wa_plan* p) {
   if (p->d_ws) cudaFree(p->d_ws);
   if (p->d_bws) cudaFree(p->d_bws);
   if (p->d_stage) cudaFree(p->d_stage);
-  if (p->d_items_hg) cudaFree(p->d_items_hg);
-  for (cudaEvent_t e : p->hg_ev) cudaEventDestroy(e);
+  if (p->d_items_pc) cudaFree(p->d_items_pc);
+  for (cudaEvent_t e : p->pc_ev) cudaEventDestroy(e);
   if (p->s_in) cudaStreamDestroy(p->s_in);
   if (p->s_out) cudaStreamDestroy(p->s_out);
+  if (p->s_c2) cudaStreamDestroy(p->s_c2);
   if (p->d_err) cudaFree(p->d_err);
   if (p->done) cudaEventDestroy(p->done);
   for (cudaEvent_t e : p->prof_ev) cudaEventDestroy(e);
@@ -537,46 +543,109 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
 
 namespace {
 
+// Frame chunks per piece after the first, which holds the chunks the first window group reads plus kPieceChunks - 1.
+// Measured at 56 heads x 99,968 rows (one copy per row range runs at the full 211 GB/s host-to-device rate): 1 chunk
+// 24.2 ms, 2 chunks 24.5, 4 chunks 25.4; head groups copied as strided blocks took 27.4 ms.
+constexpr int kPieceChunks = 1;
+
 // Lazily set up what wa_forward_host needs; called with plan->mu held.
 wa_status prepare_host_path(wa_plan_t* plan, size_t span_bytes) {
   const wa::Geometry& g = plan->hp.geo;
   const wa_layout_t& l = g.layout;
   if (plan->d_stage) return WA_OK;
-  // Head groups: heads adjacent in memory (stride_h == D) and batch entries one sequence apart let a group's rows be
-  // copied as one strided 2-D block; otherwise the whole tensor is one group.
-  const bool groupable = l.stride_h == l.D && l.stride_b == g.L * l.stride_l;
-  const int n_groups = groupable ? std::min(l.H, 6) : 1;  // 6: measured best at H3 (4: 32.3, 8: 28.7, 12: 33.2 ms)
-  plan->hg_first.assign(n_groups + 1, 0);
-  for (int i = 0; i <= n_groups; ++i) plan->hg_first[i] = (int)((int64_t)l.H * i / n_groups);
+  // With the heads of a row adjacent (stride_h == D), a range of sequence rows of one batch entry is one strided
+  // 2-D block, copied at full speed. Otherwise the tensors are copied whole as one piece.
+  plan->pc_rows = l.H == 1 || l.stride_h == l.D;
+  plan->pc_lo.clear();
+  plan->pc_hi.clear();
+  if (!plan->pc_rows) {
+    plan->pc_lo.push_back(0);
+    plan->pc_hi.push_back(g.L);
+  } else {
+    // The globals first (every window item reads them), then the frames in chunk order.
+    if (g.G > 0) {
+      plan->pc_lo.push_back(g.g0);
+      plan->pc_hi.push_back(g.g0 + g.G);
+    }
+    const int64_t KS = (int64_t)g.K * g.S;
+    int64_t c = 0;
+    while (c < g.nc) {
+      const int64_t c1 = std::min<int64_t>(g.nc, c == 0 ? g.r + 1 + kPieceChunks - 1 : c + kPieceChunks);
+      plan->pc_lo.push_back(g.f0 + c * KS);
+      plan->pc_hi.push_back(g.f0 + std::min<int64_t>(g.F, c1 * KS));
+      c = c1;
+    }
+  }
+  const int n_pieces = (int)plan->pc_lo.size();
+  // The launch of an item: the latest piece among those holding a row it reads.
+  auto last_piece = [&](int64_t lo, int64_t hi) {
+    int last = 0;
+    if (hi <= lo) return last;
+    for (int p = 0; p < n_pieces; ++p)
+      if (plan->pc_lo[p] < hi && lo < plan->pc_hi[p]) last = p;
+    return last;
+  };
+  auto launch_of = [&](const wa::Item& it) {
+    return std::max(last_piece(it.q_lo, it.q_hi), std::max(last_piece(it.s0_lo, it.s0_hi), last_piece(it.s1_lo, it.s1_hi)));
+  };
+  std::vector<std::vector<wa::Item>> by_launch(n_pieces);
+  for (const wa::Item& it : plan->hp.items) by_launch[launch_of(it)].push_back(it);  // keeps longest-first order
   std::vector<wa::Item> regrouped;
   regrouped.reserve(plan->hp.items.size());
-  plan->hg_item_off.assign(n_groups + 1, 0);
-  for (int gi = 0; gi < n_groups; ++gi) {  // keep the longest-first order inside each group
-    for (const wa::Item& it : plan->hp.items) {
-      const int h = it.bh % l.H;
-      if (h >= plan->hg_first[gi] && h < plan->hg_first[gi + 1]) regrouped.push_back(it);
+  plan->pc_item_off.assign(n_pieces + 1, 0);
+  for (int p = 0; p < n_pieces; ++p) {
+    regrouped.insert(regrouped.end(), by_launch[p].begin(), by_launch[p].end());
+    plan->pc_item_off[p + 1] = (int)regrouped.size();
+  }
+  // A window group's rows of out are complete after the launch of its items (the same launch for all of them: they
+  // read the same rows). Adjacent groups finished by one launch are copied back as one range.
+  plan->pc_out.assign(n_pieces, {});
+  if (plan->pc_rows) {
+    for (const wa_group_t& gr : plan->hp.groups) {
+      wa::Item probe{0, -1, (int32_t)gr.q_lo, (int32_t)gr.q_hi, (int32_t)gr.kv0_lo, (int32_t)gr.kv0_hi,
+                     (int32_t)gr.kv1_lo, (int32_t)gr.kv1_hi};
+      auto& ranges = plan->pc_out[launch_of(probe)];
+      if (!ranges.empty() && ranges.back().second == gr.q_lo)
+        ranges.back().second = gr.q_hi;
+      else
+        ranges.emplace_back(gr.q_lo, gr.q_hi);
     }
-    plan->hg_item_off[gi + 1] = (int)regrouped.size();
   }
   cudaError_t e = dev_alloc(&plan->d_stage, 4 * span_bytes);
-  if (e == cudaSuccess) e = dev_alloc(&plan->d_items_hg, std::max<size_t>(1, regrouped.size()) * sizeof(wa::Item));
+  if (e == cudaSuccess) e = dev_alloc(&plan->d_items_pc, std::max<size_t>(1, regrouped.size()) * sizeof(wa::Item));
   if (e != cudaSuccess) {
     cudaGetLastError();
     if (plan->d_stage) cudaFree(plan->d_stage);
     plan->d_stage = nullptr;
-    if (plan->d_items_hg) cudaFree(plan->d_items_hg);
-    plan->d_items_hg = nullptr;
+    if (plan->d_items_pc) cudaFree(plan->d_items_pc);
+    plan->d_items_pc = nullptr;
     return e == cudaErrorMemoryAllocation ? WA_ERR_OOM : WA_ERR_CUDA;
   }
-  if (cudaMemcpy(plan->d_items_hg, regrouped.data(), regrouped.size() * sizeof(wa::Item), cudaMemcpyHostToDevice) !=
+  if (cudaMemcpy(plan->d_items_pc, regrouped.data(), regrouped.size() * sizeof(wa::Item), cudaMemcpyHostToDevice) !=
           cudaSuccess ||
       cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking) != cudaSuccess)
+      cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&plan->s_c2, cudaStreamNonBlocking) != cudaSuccess)
     return WA_ERR_CUDA;
-  plan->hg_ev.resize(2 * n_groups + 2);
-  for (cudaEvent_t& ev : plan->hg_ev)
+  plan->pc_ev.resize(2 * n_pieces + 4);
+  for (cudaEvent_t& ev : plan->pc_ev)
     if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return WA_ERR_CUDA;
   return WA_OK;
+}
+
+// Copy sequence rows [lo, hi) of every batch entry (all heads) between two buffers of the plan's layout.
+cudaError_t copy_rows(const wa::Geometry& g, void* dst, const void* src, int64_t lo, int64_t hi, cudaMemcpyKind kind,
+                      cudaStream_t st) {
+  const wa_layout_t& l = g.layout;
+  const size_t width = (size_t)((l.H - 1) * l.stride_h + l.D) * 2;
+  const size_t pitch = std::max<size_t>((size_t)l.stride_l * 2, width);
+  for (int b = 0; b < l.B; ++b) {
+    const size_t off = (size_t)(b * l.stride_b + lo * l.stride_l) * 2;
+    cudaError_t e = cudaMemcpy2DAsync((uint8_t*)dst + off, pitch, (const uint8_t*)src + off, pitch, width,
+                                      (size_t)(hi - lo), kind, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -609,54 +678,60 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
   uint8_t* dk = dq + stage_span;
   uint8_t* dv = dk + stage_span;
   uint8_t* dout = dv + stage_span;
-  const int n_groups = (int)plan->hg_first.size() - 1;
-  cudaEvent_t* ev_in = &plan->hg_ev[0];
-  cudaEvent_t* ev_comp = &plan->hg_ev[n_groups];
-  cudaEvent_t ev_start = plan->hg_ev[2 * n_groups], ev_outdone = plan->hg_ev[2 * n_groups + 1];
-  // The copy streams start behind everything already queued on the caller's stream (earlier users of the staging).
+  const int n_pieces = (int)plan->pc_lo.size();
+  cudaEvent_t* ev_in = &plan->pc_ev[0];
+  cudaEvent_t* ev_comp = &plan->pc_ev[n_pieces];
+  cudaEvent_t ev_start = plan->pc_ev[2 * n_pieces], ev_c2 = plan->pc_ev[2 * n_pieces + 1];
+  cudaEvent_t ev_merged = plan->pc_ev[2 * n_pieces + 2], ev_outdone = plan->pc_ev[2 * n_pieces + 3];
+  // The helper streams start behind everything already queued on the caller's stream (earlier users of the staging).
   if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(plan->s_in, ev_start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(plan->s_out, ev_start, 0) != cudaSuccess)
+      cudaStreamWaitEvent(plan->s_out, ev_start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(plan->s_c2, ev_start, 0) != cudaSuccess)
     return WA_ERR_CUDA;
-  const size_t pitch = (size_t)l.stride_l * 2;
-  for (int gi = 0; gi < n_groups; ++gi) {
-    const int h0 = plan->hg_first[gi], nh = plan->hg_first[gi + 1] - h0;
-    const size_t off = (size_t)h0 * l.stride_h * 2;
-    // copies in: one strided block per tensor (B*L rows of nh*D elements), or the whole span for one group
-    const void* src[3] = {q, k, v};
-    uint8_t* dst[3] = {dq, dk, dv};
+  const void* src[3] = {q, k, v};
+  uint8_t* dst[3] = {dq, dk, dv};
+  wa::LaunchArgs a;
+  a.q = dq; a.k = dk; a.v = dv; a.out = dout;
+  a.ws_o = plan->d_ws;
+  a.ws_lse = plan->d_ws ? plan->d_ws + plan->ws_o_elems : nullptr;
+  a.err = plan->d_err;
+  a.n_splits = plan->hp.n_splits;
+  a.debug_flags = 0;
+  a.geo = &g;
+  for (int p = 0; p < n_pieces; ++p) {
     for (int x = 0; x < 3; ++x) {
-      cudaError_t e = n_groups > 1
-                          ? cudaMemcpy2DAsync(dst[x] + off, pitch, (const uint8_t*)src[x] + off, pitch,
-                                              (size_t)nh * l.D * 2, (size_t)l.B * g.L, cudaMemcpyHostToDevice,
-                                              plan->s_in)
+      cudaError_t e = plan->pc_rows
+                          ? copy_rows(g, dst[x], src[x], plan->pc_lo[p], plan->pc_hi[p], cudaMemcpyHostToDevice,
+                                      plan->s_in)
                           : cudaMemcpyAsync(dst[x], src[x], span, cudaMemcpyHostToDevice, plan->s_in);
       if (e != cudaSuccess) return WA_ERR_CUDA;
     }
-    if (cudaEventRecord(ev_in[gi], plan->s_in) != cudaSuccess || cudaStreamWaitEvent(s, ev_in[gi], 0) != cudaSuccess)
+    // Launches alternate between two streams, so that one launch's last items overlap the next launch's first.
+    cudaStream_t cs = (p & 1) ? plan->s_c2 : s;
+    if (cudaEventRecord(ev_in[p], plan->s_in) != cudaSuccess || cudaStreamWaitEvent(cs, ev_in[p], 0) != cudaSuccess)
       return WA_ERR_CUDA;
-    // this group's items and merge rows, on the caller's stream
-    wa::LaunchArgs a;
-    a.q = dq; a.k = dk; a.v = dv; a.out = dout;
-    a.items = plan->d_items_hg + plan->hg_item_off[gi];
-    a.n_items = plan->hg_item_off[gi + 1] - plan->hg_item_off[gi];
-    a.ws_o = plan->d_ws;
-    a.ws_lse = plan->d_ws ? plan->d_ws + plan->ws_o_elems : nullptr;
-    a.err = plan->d_err;
-    a.n_splits = plan->hp.n_splits;
-    a.debug_flags = 0;
-    a.geo = &g;
-    a.head_first = h0;
-    a.head_count = nh;
-    if (a.n_items > 0 && wa::launch_attention(a, (void*)s, plan->num_sms) != 0) return WA_ERR_CUDA;
-    if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
-    if (cudaEventRecord(ev_comp[gi], s) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_comp[gi], 0) != cudaSuccess)
+    a.items = plan->d_items_pc + plan->pc_item_off[p];
+    a.n_items = plan->pc_item_off[p + 1] - plan->pc_item_off[p];
+    if (a.n_items > 0 && wa::launch_attention(a, (void*)cs, plan->num_sms) != 0) return WA_ERR_CUDA;
+    if (plan->pc_out[p].empty()) continue;
+    if (cudaEventRecord(ev_comp[p], cs) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_comp[p], 0) != cudaSuccess)
       return WA_ERR_CUDA;
-    cudaError_t e = n_groups > 1
-                        ? cudaMemcpy2DAsync((uint8_t*)out + off, pitch, dout + off, pitch, (size_t)nh * l.D * 2,
-                                            (size_t)l.B * g.L, cudaMemcpyDeviceToHost, plan->s_out)
-                        : cudaMemcpyAsync(out, dout, span, cudaMemcpyDeviceToHost, plan->s_out);
-    if (e != cudaSuccess) return WA_ERR_CUDA;
+    for (const auto& range : plan->pc_out[p])
+      if (copy_rows(g, out, dout, range.first, range.second, cudaMemcpyDeviceToHost, plan->s_out) != cudaSuccess)
+        return WA_ERR_CUDA;
   }
+  // The merge of the global rows' splits needs every launch; then the rows not yet copied back follow.
+  if (cudaEventRecord(ev_c2, plan->s_c2) != cudaSuccess || cudaStreamWaitEvent(s, ev_c2, 0) != cudaSuccess)
+    return WA_ERR_CUDA;
+  if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
+  if (cudaEventRecord(ev_merged, s) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_merged, 0) != cudaSuccess)
+    return WA_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (!plan->pc_rows)
+    e = cudaMemcpyAsync(out, dout, span, cudaMemcpyDeviceToHost, plan->s_out);
+  else if (g.G > 0)
+    e = copy_rows(g, out, dout, g.g0, g.g0 + g.G, cudaMemcpyDeviceToHost, plan->s_out);
+  if (e != cudaSuccess) return WA_ERR_CUDA;
   if (cudaEventRecord(ev_outdone, plan->s_out) != cudaSuccess || cudaStreamWaitEvent(s, ev_outdone, 0) != cudaSuccess ||
       cudaEventRecord(plan->done, s) != cudaSuccess)
     return WA_ERR_CUDA;

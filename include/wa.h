@@ -129,10 +129,13 @@ wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const 
  * wa_forward on HOST buffers: q, k, v are read from host memory and out is written to host memory (all bf16 with
  * the plan's layout; page-locked memory lets the copies run asynchronously and overlap the computation). The
  * library keeps device copies of the four tensors in the plan (allocated by the first call: 4 x the layout's span,
- * kept until the plan is freed). When heads are adjacent in memory (stride_h == D) and batch entries are one
- * sequence apart (stride_b == L * stride_l), the heads are processed in up to 6 groups: group i+1's inputs are
- * copied in, group i is computed (on `stream`) and group i-1's rows are copied out at the same time, on two
- * library-owned copy streams chained to `stream` by events; other layouts run as one group. Results are identical
+ * kept until the plan is freed). When the heads of a sequence row are adjacent in memory (stride_h == D, or H == 1),
+ * the sequence is copied in as row pieces, the global rows first and then the frames one chunk at a time (the first
+ * piece holds the chunks the first window group reads). After each piece arrives, one launch computes the work items
+ * whose rows have all arrived, and the rows of out that launch completes are copied back while later pieces are
+ * still arriving. Launches alternate between `stream` and a library-owned compute stream; copies run on two
+ * library-owned copy streams; events chain all of them to `stream`. The global rows' merge runs last. Other
+ * layouts are copied whole and computed in one launch. Results are identical
  * to wa_forward. The call is asynchronous: out is complete when `stream` reaches this point (e.g. after
  * cudaStreamSynchronize); q, k, v and out must stay valid until then.
  * Errors: WA_ERR_INVALID for null pointers or out overlapping an input; WA_ERR_OOM when the device copies cannot

@@ -1,6 +1,7 @@
-"""wa_forward_host: the forward on host buffers, pipelined over head groups (copies in, compute, copies out on three
-streams). Its results must equal the device-resident forward bit for bit (the same kernels and work items, only
-regrouped by head), and therefore the fp64 oracle within the forward's bar."""
+"""wa_forward_host: the forward on host buffers, pipelined over pieces of the sequence (copies in, compute, copies out
+on separate streams; each launch runs the work items whose rows have arrived). Its results must equal the
+device-resident forward bit for bit (the same kernels and work items, only regrouped by launch), and therefore the
+fp64 oracle within the forward's bar."""
 import numpy as np
 import pytest
 import torch
@@ -60,6 +61,53 @@ def test_host_forward_single_group_layout(cuda):
     qh, kh, vh = (t.cpu() for t in (qs, ks, vs))
     assert strides_of(qh) == strides_of(qs)
     plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos, strides=strides_of(qs))
+    try:
+        got = plan.forward_host(qh, kh, vh)
+        assert plan.check_error() == 0
+    finally:
+        plan.close()
+    assert torch.equal(got, want)
+
+
+def host_layout(t, kind):
+    """Same logical [B, L, H, D] tensor in a physical layout whose rows are still one block of heads."""
+    B, L, H, D = t.shape
+    if kind == "rowpad":  # rows padded to a larger pitch, heads adjacent inside a row
+        big = torch.zeros(B, L, H * D + 64, dtype=t.dtype, device=t.device)
+        big[:, :, :H * D] = t.reshape(B, L, H * D)
+        return big[:, :, :H * D].unflatten(2, (H, D))
+    if kind == "lbhd":  # batch entries interleaved between sequence rows
+        return t.permute(1, 0, 2, 3).contiguous().permute(1, 0, 2, 3)
+    raise ValueError(kind)
+
+
+PIECE_CASES = [
+    (configs.Workload("host_no_globals", B=1, H=2, D=128, T=9, S=100, K=2, r=1, G=0, global_pos=0, seed=63), None),
+    (configs.Workload("host_radius_covers_all", B=1, H=2, D=128, T=7, S=90, K=2, r=9, G=40, global_pos=0, seed=64),
+     None),
+    (configs.Workload("host_radius0_front", B=2, H=2, D=64, T=8, S=70, K=3, r=0, G=200, global_pos=1, seed=65), None),
+    (configs.Workload("host_one_token_frames", B=1, H=3, D=128, T=300, S=1, K=7, r=2, G=5, global_pos=1, seed=66),
+     None),
+    (configs.Workload("host_rowpad", B=2, H=3, D=128, T=11, S=40, K=2, r=2, G=24, global_pos=0, seed=67), "rowpad"),
+    (configs.Workload("host_lbhd", B=2, H=2, D=64, T=10, S=30, K=3, r=1, G=16, global_pos=1, seed=68), "lbhd"),
+    (configs.Workload("host_one_head_rowpad", B=1, H=1, D=128, T=12, S=33, K=1, r=3, G=7, global_pos=0, seed=69),
+     "rowpad"),
+]
+
+
+@pytest.mark.parametrize("w,kind", PIECE_CASES, ids=[c[0].name for c in PIECE_CASES])
+def test_host_forward_pieces(cuda, w, kind):
+    """Geometries and row layouts that change the pieces: no globals, one group, front globals, many small chunks,
+    padded rows, batch entries between rows, a single head."""
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    if kind is not None:
+        q, k, v = (host_layout(t, kind) for t in (q, k, v))
+    want = device_forward(cuda, w, q, k, v)
+    qh, kh, vh = (torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, pin_memory=True) for t in (q, k, v))
+    for h, d in zip((qh, kh, vh), (q, k, v)):
+        h.copy_(d)
+    assert strides_of(qh) == strides_of(q)
+    plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos, strides=strides_of(q))
     try:
         got = plan.forward_host(qh, kh, vh)
         assert plan.check_error() == 0
