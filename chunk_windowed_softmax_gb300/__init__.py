@@ -19,7 +19,8 @@ STATUS = {0: "WA_OK", 1: "WA_ERR_INVALID", 2: "WA_ERR_UNSUPPORTED", 3: "WA_ERR_O
 EXPORTS = ("wa_plan_create", "wa_forward", "wa_plan_check_error", "wa_plan_info", "wa_plan_release",
            "wa_geometry_describe", "wa_status_string", "wa_plan_set_debug_flags", "wa_cache_size", "wa_plan_refcount",
            "wa_plan_profile", "wa_plan_profile_read", "wa_forward_static", "wa_forward_fp8", "wa_forward_lse",
-           "wa_backward", "wa_plan_profile_read_backward", "wa_forward_host")
+           "wa_backward", "wa_plan_profile_read_backward", "wa_forward_host",
+           "wa_host_schedule_describe")
 
 
 class WAError(RuntimeError):
@@ -84,6 +85,11 @@ def lib():
                                                                  ctypes.POINTER(wa_group_t), ctypes.c_int64,
                                                                  ctypes.POINTER(ctypes.c_int64), ctypes.c_int64]
         L.wa_geometry_describe.restype = ctypes.c_int
+        i64p, i32p = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+        L.wa_host_schedule_describe.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(wa_layout_t), i64p,
+                                                                      ctypes.c_int64, i32p, ctypes.c_int64, i64p,
+                                                                      ctypes.c_int64, i64p, i64p, i32p]
+        L.wa_host_schedule_describe.restype = ctypes.c_int
         L.wa_status_string.argtypes = [ctypes.c_int]
         L.wa_status_string.restype = ctypes.c_char_p
         L.wa_plan_set_debug_flags.argtypes = [P, ctypes.c_int]
@@ -181,6 +187,26 @@ def wa_geometry_describe(T, S, K, r, G, layout, with_groups=True, with_items=Fal
     if with_items:
         items = [tuple(ibuf[8 * i:8 * i + 8]) for i in range(info.n_items)]
     return info.as_dict(), groups, items
+
+
+def wa_host_schedule_describe(T, S, K, r, G, layout, n_items):
+    """Host-only piece schedule of the host-buffer forward: {"row_pieces": bool, "pieces": [(lo, hi)] in copy order,
+    "item_launch": [launch per work item, in wa_geometry_describe's item order], "out": [(launch, lo, hi)]}."""
+    L = lib()
+    n_pieces, n_out, rows = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    args = (T, S, K, r, G, ctypes.byref(layout))
+    _check(L.wa_host_schedule_describe(*args, None, 0, None, 0, None, 0, ctypes.byref(n_pieces), ctypes.byref(n_out),
+                                       ctypes.byref(rows)), "wa_host_schedule_describe")
+    pbuf = (ctypes.c_int64 * (2 * max(1, n_pieces.value)))()
+    lbuf = (ctypes.c_int32 * max(1, n_items))()
+    obuf = (ctypes.c_int64 * (3 * max(1, n_out.value)))()
+    _check(L.wa_host_schedule_describe(*args, pbuf, n_pieces.value, lbuf, n_items, obuf, n_out.value,
+                                       ctypes.byref(n_pieces), ctypes.byref(n_out), ctypes.byref(rows)),
+           "wa_host_schedule_describe")
+    return {"row_pieces": bool(rows.value),
+            "pieces": [(pbuf[2 * i], pbuf[2 * i + 1]) for i in range(n_pieces.value)],
+            "item_launch": list(lbuf[:n_items]),
+            "out": [tuple(obuf[3 * i:3 * i + 3]) for i in range(n_out.value)]}
 
 
 # ----------------------------------------------------------------------------------------- torch side

@@ -3,6 +3,7 @@
 
 #include <stdint.h>
 
+#include <utility>
 #include <vector>
 
 #include "../../include/wa.h"
@@ -38,10 +39,21 @@ struct HostPlan {
   int n_splits;
 };
 
+// The piece schedule of the host-buffer forward: the sequence rows copied in, piece by piece, and after piece p
+// launch p of the items whose rows have all arrived; after launch p the rows of out it completed are copied back.
+struct HostSchedule {
+  bool rows = false;                    // pieces are row blocks of all heads (else one piece: the whole tensors)
+  std::vector<int64_t> lo, hi;          // piece p: sequence rows [lo[p], hi[p]) of every batch entry, in copy order
+  std::vector<int> launch;              // per item of HostPlan::items (same order): the launch that runs it
+  std::vector<std::vector<std::pair<int64_t, int64_t>>> out;  // per launch: frame rows of out it completes
+};
+
 // Validate arguments; on success fill `geo`.
 wa_status make_geometry(int T, int S, int K, int r, int G, const wa_layout_t* layout, Geometry* geo);
 // Build groups, splits and the ordered work list on the host.
 void build_host_plan(const Geometry& geo, HostPlan* hp);
+// Build the host-buffer forward's piece schedule for a plan (host only).
+void build_host_schedule(const HostPlan& hp, HostSchedule* hs);
 
 // Arguments of one attention launch (device pointers; tensor maps are built by the launcher).
 struct LaunchArgs {

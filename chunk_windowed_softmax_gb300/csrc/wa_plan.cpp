@@ -49,10 +49,8 @@ struct wa_plan {
   // out that launch p completes are copied back while later pieces are still on their way.
   uint8_t* d_stage = nullptr;
   wa::Item* d_items_pc = nullptr;
-  bool pc_rows = false;                          // pieces are row blocks (else one piece: the whole tensors)
-  std::vector<int64_t> pc_lo, pc_hi;             // piece p: sequence rows [pc_lo[p], pc_hi[p]) of every batch entry
+  wa::HostSchedule hs;
   std::vector<int> pc_item_off;                  // launch p: items [pc_item_off[p], pc_item_off[p + 1])
-  std::vector<std::vector<std::pair<int64_t, int64_t>>> pc_out;  // out row ranges complete after launch p
   cudaStream_t s_in = nullptr, s_out = nullptr, s_c2 = nullptr;
   std::vector<cudaEvent_t> pc_ev;                // per piece: copies in, launch done; then four for the whole call
 };
@@ -183,6 +181,100 @@ void build_host_plan(const Geometry& g, HostPlan* hp) {
   in.kv_tiles = kt;
 }
 
+
+// At most this many pieces (and launches) per host-buffer forward; geometries with more window groups merge
+// neighbouring pieces.
+constexpr int kMaxPieces = 64;
+
+// One past the last sequence row that the attention kernel reads for the row range [lo, hi): it reads whole 128-row
+// tiles from the start of the range, so the last tile also reads rows past its end (rows past L read as zeros).
+// Those scores are masked, but 0 times a row that has not arrived yet could be NaN, so those rows must have arrived.
+static int64_t read_end(const Geometry& g, int64_t lo, int64_t hi) {
+  return hi > lo ? std::min<int64_t>(g.L, lo + cdiv(hi - lo, kTileRows) * kTileRows) : lo;
+}
+
+void build_host_schedule(const HostPlan& hp, HostSchedule* hs) {
+  const Geometry& g = hp.geo;
+  const wa_layout_t& l = g.layout;
+  // With the heads of a row adjacent (stride_h == D), a range of sequence rows of one batch entry is one strided
+  // 2-D block, copied at full speed. Otherwise the tensors are copied whole as one piece.
+  hs->rows = l.H == 1 || l.stride_h == l.D;
+  hs->lo.clear();
+  hs->hi.clear();
+  if (!hs->rows) {
+    hs->lo.push_back(0);
+    hs->hi.push_back(g.L);
+  } else {
+    // The globals first (every window item reads them), then the frames in order, cut where a window group's reads
+    // end: each group can start as soon as the piece holding its last row has arrived. Measured at 56 heads x
+    // 99,968 rows (34 groups of one chunk; a row block copies at the full 211 GB/s host-to-device rate): 24.2 ms
+    // with one chunk per piece, 24.5 with two, 25.4 with four; head groups copied as strided blocks took 27.4 ms.
+    if (g.G > 0) {
+      hs->lo.push_back(g.g0);
+      hs->hi.push_back(g.g0 + g.G);
+    }
+    const int64_t f_lo = g.f0, f_hi = g.f0 + g.F;
+    // The last frame row read for [lo, hi), plus one (f_lo when the reads hold no frame row, e.g. the globals).
+    auto frame_end = [&](int64_t lo, int64_t hi) {
+      const int64_t e = std::min(read_end(g, lo, hi), f_hi);
+      return hi > lo && std::max(lo, f_lo) < e ? e : f_lo;
+    };
+    std::vector<int64_t> cuts;  // increasing frame rows where pieces end
+    for (const wa_group_t& gr : hp.groups) {
+      const int64_t q_last = gr.q_lo + (gr.q_hi - gr.q_lo - 1) / kItemRows * kItemRows;  // the last item's rows
+      const int64_t end = std::max({frame_end(gr.kv0_lo, gr.kv0_hi), frame_end(gr.kv1_lo, gr.kv1_hi),
+                                    frame_end(q_last, gr.q_hi), f_lo + 1});
+      if (cuts.empty() || end > cuts.back()) cuts.push_back(end);
+    }
+    if (cuts.empty() || cuts.back() != f_hi) cuts.push_back(f_hi);
+    const int max_frame_pieces = kMaxPieces - (g.G > 0 ? 1 : 0);
+    const int n_cuts = (int)cuts.size();
+    int64_t lo = f_lo;
+    for (int i = 0; i < std::min(n_cuts, max_frame_pieces); ++i) {
+      // every cut when they fit, else evenly spaced ones (always including the last)
+      const int64_t hi =
+          n_cuts <= max_frame_pieces ? cuts[i] : cuts[(int64_t)(i + 1) * n_cuts / max_frame_pieces - 1];
+      hs->lo.push_back(lo);
+      hs->hi.push_back(hi);
+      lo = hi;
+    }
+  }
+  const int n_pieces = (int)hs->lo.size();
+  // The launch of an item: the latest piece among those holding a row it reads.
+  auto last_piece = [&](int64_t lo, int64_t hi) {
+    int last = 0;
+    if (hi <= lo) return last;
+    hi = read_end(g, lo, hi);
+    for (int p = 0; p < n_pieces; ++p)
+      if (hs->lo[p] < hi && lo < hs->hi[p]) last = p;
+    return last;
+  };
+  auto launch_of = [&](const Item& it) {
+    return std::max({last_piece(it.q_lo, it.q_hi), last_piece(it.s0_lo, it.s0_hi), last_piece(it.s1_lo, it.s1_hi)});
+  };
+  hs->launch.resize(hp.items.size());
+  for (size_t i = 0; i < hp.items.size(); ++i) hs->launch[i] = launch_of(hp.items[i]);
+  // A window group's rows of out are complete after the launch of its items (the same launch for all of them: they
+  // read the same rows). Adjacent groups finished by one launch are copied back as one range. Without row pieces
+  // the whole of out is copied back at the end instead.
+  hs->out.assign(n_pieces, {});
+  if (hs->rows) {
+    for (const wa_group_t& gr : hp.groups) {
+      int launch = 0;
+      for (int64_t q = gr.q_lo; q < gr.q_hi; q += kItemRows) {
+        const Item it{0, -1, (int32_t)q, (int32_t)std::min<int64_t>(gr.q_hi, q + kItemRows), (int32_t)gr.kv0_lo,
+                      (int32_t)gr.kv0_hi, (int32_t)gr.kv1_lo, (int32_t)gr.kv1_hi};
+        launch = std::max(launch, launch_of(it));
+      }
+      auto& ranges = hs->out[launch];
+      if (!ranges.empty() && ranges.back().second == gr.q_lo)
+        ranges.back().second = gr.q_hi;
+      else
+        ranges.emplace_back(gr.q_lo, gr.q_hi);
+    }
+  }
+}
+
 }  // namespace wa
 
 // ------------------------------------------------------------------------------------------- plan cache
@@ -311,6 +403,40 @@ wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layou
       o[0] = it.bh; o[1] = it.split < 0 ? 0 : 1; o[2] = it.q_lo; o[3] = it.q_hi;
       o[4] = it.s0_lo; o[5] = it.s0_hi; o[6] = it.s1_lo; o[7] = it.s1_hi;
     }
+  return WA_OK;
+}
+
+wa_status wa_host_schedule_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, int64_t* pieces,
+                                    int64_t pieces_cap, int32_t* item_launch, int64_t items_cap, int64_t* out_ranges,
+                                    int64_t out_cap, int64_t* n_pieces, int64_t* n_out, int32_t* row_pieces) {
+  if (!n_pieces || !n_out || !row_pieces) return WA_ERR_INVALID;
+  wa::Geometry g;
+  wa_status st = wa::make_geometry(T, S, K, r, G, layout, &g);
+  if (st != WA_OK) return st;
+  wa::HostPlan hp;
+  wa::build_host_plan(g, &hp);
+  wa::HostSchedule hs;
+  wa::build_host_schedule(hp, &hs);
+  *n_pieces = (int64_t)hs.lo.size();
+  *row_pieces = hs.rows ? 1 : 0;
+  if (pieces)
+    for (int64_t i = 0; i < std::min<int64_t>(pieces_cap, *n_pieces); ++i) {
+      pieces[2 * i] = hs.lo[i];
+      pieces[2 * i + 1] = hs.hi[i];
+    }
+  if (item_launch)
+    for (int64_t i = 0; i < std::min<int64_t>(items_cap, (int64_t)hs.launch.size()); ++i) item_launch[i] = hs.launch[i];
+  int64_t n = 0;
+  for (size_t p = 0; p < hs.out.size(); ++p)
+    for (const auto& range : hs.out[p]) {
+      if (out_ranges && n < out_cap) {
+        out_ranges[3 * n] = (int64_t)p;
+        out_ranges[3 * n + 1] = range.first;
+        out_ranges[3 * n + 2] = range.second;
+      }
+      ++n;
+    }
+  *n_out = n;
   return WA_OK;
 }
 
@@ -543,73 +669,20 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
 
 namespace {
 
-// Frame chunks per piece after the first, which holds the chunks the first window group reads plus kPieceChunks - 1.
-// Measured at 56 heads x 99,968 rows (one copy per row range runs at the full 211 GB/s host-to-device rate): 1 chunk
-// 24.2 ms, 2 chunks 24.5, 4 chunks 25.4; head groups copied as strided blocks took 27.4 ms.
-constexpr int kPieceChunks = 1;
-
 // Lazily set up what wa_forward_host needs; called with plan->mu held.
 wa_status prepare_host_path(wa_plan_t* plan, size_t span_bytes) {
-  const wa::Geometry& g = plan->hp.geo;
-  const wa_layout_t& l = g.layout;
   if (plan->d_stage) return WA_OK;
-  // With the heads of a row adjacent (stride_h == D), a range of sequence rows of one batch entry is one strided
-  // 2-D block, copied at full speed. Otherwise the tensors are copied whole as one piece.
-  plan->pc_rows = l.H == 1 || l.stride_h == l.D;
-  plan->pc_lo.clear();
-  plan->pc_hi.clear();
-  if (!plan->pc_rows) {
-    plan->pc_lo.push_back(0);
-    plan->pc_hi.push_back(g.L);
-  } else {
-    // The globals first (every window item reads them), then the frames in chunk order.
-    if (g.G > 0) {
-      plan->pc_lo.push_back(g.g0);
-      plan->pc_hi.push_back(g.g0 + g.G);
-    }
-    const int64_t KS = (int64_t)g.K * g.S;
-    int64_t c = 0;
-    while (c < g.nc) {
-      const int64_t c1 = std::min<int64_t>(g.nc, c == 0 ? g.r + 1 + kPieceChunks - 1 : c + kPieceChunks);
-      plan->pc_lo.push_back(g.f0 + c * KS);
-      plan->pc_hi.push_back(g.f0 + std::min<int64_t>(g.F, c1 * KS));
-      c = c1;
-    }
-  }
-  const int n_pieces = (int)plan->pc_lo.size();
-  // The launch of an item: the latest piece among those holding a row it reads.
-  auto last_piece = [&](int64_t lo, int64_t hi) {
-    int last = 0;
-    if (hi <= lo) return last;
-    for (int p = 0; p < n_pieces; ++p)
-      if (plan->pc_lo[p] < hi && lo < plan->pc_hi[p]) last = p;
-    return last;
-  };
-  auto launch_of = [&](const wa::Item& it) {
-    return std::max(last_piece(it.q_lo, it.q_hi), std::max(last_piece(it.s0_lo, it.s0_hi), last_piece(it.s1_lo, it.s1_hi)));
-  };
+  wa::build_host_schedule(plan->hp, &plan->hs);
+  const int n_pieces = (int)plan->hs.lo.size();
   std::vector<std::vector<wa::Item>> by_launch(n_pieces);
-  for (const wa::Item& it : plan->hp.items) by_launch[launch_of(it)].push_back(it);  // keeps longest-first order
+  for (size_t i = 0; i < plan->hp.items.size(); ++i)  // keeps the longest-first order inside each launch
+    by_launch[plan->hs.launch[i]].push_back(plan->hp.items[i]);
   std::vector<wa::Item> regrouped;
   regrouped.reserve(plan->hp.items.size());
   plan->pc_item_off.assign(n_pieces + 1, 0);
   for (int p = 0; p < n_pieces; ++p) {
     regrouped.insert(regrouped.end(), by_launch[p].begin(), by_launch[p].end());
     plan->pc_item_off[p + 1] = (int)regrouped.size();
-  }
-  // A window group's rows of out are complete after the launch of its items (the same launch for all of them: they
-  // read the same rows). Adjacent groups finished by one launch are copied back as one range.
-  plan->pc_out.assign(n_pieces, {});
-  if (plan->pc_rows) {
-    for (const wa_group_t& gr : plan->hp.groups) {
-      wa::Item probe{0, -1, (int32_t)gr.q_lo, (int32_t)gr.q_hi, (int32_t)gr.kv0_lo, (int32_t)gr.kv0_hi,
-                     (int32_t)gr.kv1_lo, (int32_t)gr.kv1_hi};
-      auto& ranges = plan->pc_out[launch_of(probe)];
-      if (!ranges.empty() && ranges.back().second == gr.q_lo)
-        ranges.back().second = gr.q_hi;
-      else
-        ranges.emplace_back(gr.q_lo, gr.q_hi);
-    }
   }
   cudaError_t e = dev_alloc(&plan->d_stage, 4 * span_bytes);
   if (e == cudaSuccess) e = dev_alloc(&plan->d_items_pc, std::max<size_t>(1, regrouped.size()) * sizeof(wa::Item));
@@ -678,7 +751,7 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
   uint8_t* dk = dq + stage_span;
   uint8_t* dv = dk + stage_span;
   uint8_t* dout = dv + stage_span;
-  const int n_pieces = (int)plan->pc_lo.size();
+  const int n_pieces = (int)plan->hs.lo.size();
   cudaEvent_t* ev_in = &plan->pc_ev[0];
   cudaEvent_t* ev_comp = &plan->pc_ev[n_pieces];
   cudaEvent_t ev_start = plan->pc_ev[2 * n_pieces], ev_c2 = plan->pc_ev[2 * n_pieces + 1];
@@ -700,8 +773,8 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
   a.geo = &g;
   for (int p = 0; p < n_pieces; ++p) {
     for (int x = 0; x < 3; ++x) {
-      cudaError_t e = plan->pc_rows
-                          ? copy_rows(g, dst[x], src[x], plan->pc_lo[p], plan->pc_hi[p], cudaMemcpyHostToDevice,
+      cudaError_t e = plan->hs.rows
+                          ? copy_rows(g, dst[x], src[x], plan->hs.lo[p], plan->hs.hi[p], cudaMemcpyHostToDevice,
                                       plan->s_in)
                           : cudaMemcpyAsync(dst[x], src[x], span, cudaMemcpyHostToDevice, plan->s_in);
       if (e != cudaSuccess) return WA_ERR_CUDA;
@@ -713,10 +786,10 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
     a.items = plan->d_items_pc + plan->pc_item_off[p];
     a.n_items = plan->pc_item_off[p + 1] - plan->pc_item_off[p];
     if (a.n_items > 0 && wa::launch_attention(a, (void*)cs, plan->num_sms) != 0) return WA_ERR_CUDA;
-    if (plan->pc_out[p].empty()) continue;
+    if (plan->hs.out[p].empty()) continue;
     if (cudaEventRecord(ev_comp[p], cs) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_comp[p], 0) != cudaSuccess)
       return WA_ERR_CUDA;
-    for (const auto& range : plan->pc_out[p])
+    for (const auto& range : plan->hs.out[p])
       if (copy_rows(g, out, dout, range.first, range.second, cudaMemcpyDeviceToHost, plan->s_out) != cudaSuccess)
         return WA_ERR_CUDA;
   }
@@ -727,7 +800,7 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
   if (cudaEventRecord(ev_merged, s) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_merged, 0) != cudaSuccess)
     return WA_ERR_CUDA;
   cudaError_t e = cudaSuccess;
-  if (!plan->pc_rows)
+  if (!plan->hs.rows)
     e = cudaMemcpyAsync(out, dout, span, cudaMemcpyDeviceToHost, plan->s_out);
   else if (g.G > 0)
     e = copy_rows(g, out, dout, g.g0, g.g0 + g.G, cudaMemcpyDeviceToHost, plan->s_out);

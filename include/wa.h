@@ -185,6 +185,21 @@ void wa_plan_release(wa_plan_t* plan);
 wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, wa_plan_info_t* info,
                                wa_group_t* groups, int64_t groups_cap, int64_t* items, int64_t items_cap);
 
+/*
+ * Host-only: the piece schedule wa_forward_host uses for this geometry and layout, without touching any device.
+ * Pieces are sequence row ranges (all batch entries and heads) in the order they are copied in; after piece p has
+ * arrived, launch p runs the work items whose rows have all arrived; after launch p the frame rows of out that it
+ * completed are copied back (the global rows, or the whole of out when the pieces are not row blocks, after the
+ * merge). Writes min(n_pieces, pieces_cap) pairs {lo, hi} to `pieces`; for each work item, in wa_geometry_describe's
+ * order, min(n_items, items_cap) launch indices to `item_launch`; and min(n_out, out_cap) triples {launch, lo, hi}
+ * to `out_ranges`. Any of the three may be NULL. *n_pieces and *n_out receive the full counts; *row_pieces is 1
+ * when pieces are row blocks (stride_h == D or H == 1), else 0 (one piece: the whole tensors).
+ * Errors: as wa_plan_create for the arguments, WA_ERR_INVALID for a null count pointer.
+ */
+wa_status wa_host_schedule_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, int64_t* pieces,
+                                    int64_t pieces_cap, int32_t* item_launch, int64_t items_cap, int64_t* out_ranges,
+                                    int64_t out_cap, int64_t* n_pieces, int64_t* n_out, int32_t* row_pieces);
+
 /* Static string for a status code ("WA_OK", ...); "WA_UNKNOWN" for other values. */
 const char* wa_status_string(wa_status s);
 

@@ -13,6 +13,14 @@ from test_parity_gpu import check_slices, relayout, strides_of
 pytestmark = pytest.mark.gpu
 
 
+def prime_with_nan(plan, q):
+    """Run one host forward on all-NaN inputs, so that the plan's device staging holds NaN wherever the next call has
+    not copied its own rows yet: a launch that reads a row before it has arrived then shows NaN in its output."""
+    nan = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, pin_memory=q.is_pinned()).fill_(float("nan"))
+    plan.forward_host(nan, nan, nan)
+    assert plan.check_error() == 0
+
+
 def device_forward(wa, w, q, k, v):
     plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos, strides=strides_of(q))
     try:
@@ -34,6 +42,7 @@ def test_host_forward_matches_device_forward(cuda, w, pinned):
     qh, kh, vh = (t.cpu().pin_memory() if pinned else t.cpu() for t in (q, k, v))
     plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
     try:
+        prime_with_nan(plan, qh)
         got = plan.forward_host(qh, kh, vh)
         again = plan.forward_host(qh, kh, vh)  # the staging buffers are reused
         assert plan.check_error() == 0
@@ -109,6 +118,7 @@ def test_host_forward_pieces(cuda, w, kind):
     assert strides_of(qh) == strides_of(q)
     plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos, strides=strides_of(q))
     try:
+        prime_with_nan(plan, qh)
         got = plan.forward_host(qh, kh, vh)
         assert plan.check_error() == 0
     finally:

@@ -1,0 +1,127 @@
+"""The host-buffer forward's piece schedule (host only, no GPU).
+
+The sequence is copied in as row pieces and launch p runs after piece p has arrived, so the schedule is correct when
+- the pieces partition the rows [0, L) (every row copied exactly once), the global rows first;
+- every work item runs in the launch of the latest piece holding a row it reads, where the kernel reads whole
+  128-row tiles from the start of each of its ranges (q rows, key segment 0, key segment 1; rows past L read as
+  zeros): earlier would read rows that have not arrived, later would stall the pipeline;
+- every frame row of out is copied back exactly once, after every item that writes it has run (the global rows are
+  copied after the merge);
+and it pipelines: at H3 sizes one piece per window group, the first frame piece no longer than the first group needs.
+"""
+import numpy as np
+import pytest
+
+import chunk_windowed_softmax_gb300 as wa
+from chunk_windowed_softmax_gb300 import configs
+
+TILE = 128
+
+
+def describe(T, S, K, r, G, B, H, D, global_pos, strides=None):
+    L = T * S + G
+    layout = wa.make_layout(B, L, H, D, global_pos, strides)
+    info, groups, items = wa.wa_geometry_describe(T, S, K, r, G, layout, with_groups=True, with_items=True)
+    sched = wa.wa_host_schedule_describe(T, S, K, r, G, layout, info["n_items"])
+    return L, info, groups, items, sched
+
+
+def read_ranges(item, L):
+    """Rows the kernel reads for one work item: whole tiles from the start of each range, capped at L."""
+    out = []
+    for lo, hi in ((item[2], item[3]), (item[4], item[5]), (item[6], item[7])):
+        if hi > lo:
+            out.append((lo, min(L, lo + -(-(hi - lo) // TILE) * TILE)))
+    return out
+
+
+def check_schedule(T, S, K, r, G, B, H, D, global_pos, strides=None):
+    L, info, groups, items, sched = describe(T, S, K, r, G, B, H, D, global_pos, strides)
+    pieces, launch = sched["pieces"], sched["item_launch"]
+    F = T * S
+    g0, f0 = (0, G) if global_pos else (F, 0)
+    # pieces partition [0, L)
+    piece_of = np.full(L, -1)
+    for p, (lo, hi) in enumerate(pieces):
+        assert 0 <= lo < hi <= L
+        assert (piece_of[lo:hi] == -1).all(), "pieces overlap"
+        piece_of[lo:hi] = p
+    assert (piece_of >= 0).all(), "a row is never copied"
+    if sched["row_pieces"] and G > 0:
+        assert pieces[0] == (g0, g0 + G)
+    # each item runs exactly when the last piece it reads has arrived
+    assert len(launch) == len(items)
+    for it, p in zip(items, launch):
+        need = max(int(piece_of[lo:hi].max()) for lo, hi in read_ranges(it, L))
+        assert p == need, (it, p, need)
+    # out rows: each frame row copied back once, after all its writers
+    if sched["row_pieces"]:
+        copied = np.full(L, -1)
+        for p, lo, hi in sched["out"]:
+            assert f0 <= lo < hi <= f0 + F
+            assert (copied[lo:hi] == -1).all(), "a row of out is copied back twice"
+            copied[lo:hi] = p
+        assert (copied[f0:f0 + F] >= 0).all(), "a frame row of out is never copied back"
+        for it, p in zip(items, launch):
+            if it[1] == 0:  # window item: writes out rows [q_lo, q_hi)
+                assert (copied[it[2]:it[3]] >= p).all(), "out rows copied back before their item ran"
+    else:
+        assert pieces == [(0, L)] and sched["out"] == [] and set(launch) <= {0}
+    return L, info, groups, sched
+
+
+GEOMETRIES = [
+    (6, 16, 2, 1, 8, 1, 2, 64, 0),        # Tiny
+    (24, 256, 4, 1, 256, 1, 8, 128, 0),   # Medium
+    (50, 300, 4, 2, 77, 2, 16, 128, 1),   # Ragged (front globals, two batch entries)
+    (9, 100, 2, 1, 0, 1, 2, 128, 0),      # no globals
+    (7, 90, 2, 9, 40, 1, 2, 128, 0),      # the radius covers every chunk: one group
+    (8, 70, 3, 0, 200, 2, 2, 64, 1),      # radius 0, front globals
+    (3, 50, 5, 1, 9, 1, 2, 128, 0),       # one chunk longer than T
+    (300, 1, 7, 2, 5, 1, 3, 128, 1),      # one-token frames
+    (11, 40, 2, 2, 24, 2, 3, 128, 0),
+    (5, 200, 1, 0, 300, 1, 1, 64, 0),     # r = 0: each group's last query tile reads past its own chunk
+]
+
+
+@pytest.mark.parametrize("geo", GEOMETRIES, ids=lambda g: "T{}_S{}_K{}_r{}_G{}_B{}_H{}_D{}_p{}".format(*g))
+def test_schedule_is_valid(geo):
+    check_schedule(*geo)
+
+
+def test_schedule_row_padded_and_batch_interleaved_layouts():
+    T, S, K, r, G, B, H, D = 11, 40, 2, 2, 24, 2, 3, 128
+    L = T * S + G
+    check_schedule(T, S, K, r, G, B, H, D, 0, strides=(L * (H * D + 64), H * D + 64, D))  # padded rows
+    check_schedule(T, S, K, r, G, B, H, D, 1, strides=(H * D, B * H * D, D))  # batch entries between rows
+
+
+def test_schedule_single_piece_when_heads_are_not_adjacent():
+    T, S, K, r, G, B, H, D = 6, 50, 2, 1, 20, 2, 3, 128
+    L = T * S + G
+    _, _, _, sched = check_schedule(T, S, K, r, G, B, H, D, 1, strides=(H * L * D, D, L * D))  # [B, H, L, D]
+    assert not sched["row_pieces"]
+
+
+def test_schedule_pipelines_h3():
+    w = configs.H3
+    L, info, groups, sched = check_schedule(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    KS = w.K * w.S
+    pieces = sched["pieces"]
+    assert sched["row_pieces"]
+    # the globals, then one piece per window group, ending where its reads end; the last two groups (windows
+    # [31, 33] and [32, 33]) both read to the end of the frames and share the last piece
+    assert info["n_groups"] == 34 and len(pieces) == 1 + 33
+    # the first frame piece: the chunks the first group reads (chunks 0..r) and at most one tile more
+    assert pieces[1][0] == 0 and (w.r + 1) * KS <= pieces[1][1] <= (w.r + 1) * KS + TILE
+    # later frame pieces hold about one chunk each
+    assert all(abs((hi - lo) - KS) <= TILE for lo, hi in pieces[2:-1])
+    launches = sched["item_launch"]
+    assert max(launches) == len(pieces) - 1 and min(launches) >= 1  # piece 0 (globals) alone runs nothing
+
+
+def test_schedule_caps_the_piece_count():
+    # 400 one-token chunks with r = 0: 400 window groups, merged into at most 64 pieces
+    L, info, groups, sched = check_schedule(400, 1, 1, 0, 3, 1, 2, 64, 0)
+    assert info["n_groups"] == 400
+    assert len(sched["pieces"]) == 64
