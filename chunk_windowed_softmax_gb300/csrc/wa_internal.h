@@ -74,6 +74,8 @@ struct LaunchArgs {
   float qk_scale = 1.0f;   // dequantisation factor of the scores: q_scale * k_scale (1 for bf16 inputs)
   int head_first = 0;      // the merge covers the heads [head_first, head_first + head_count) of every batch entry
   int head_count = 0;      // (0: all heads)
+  int* item_counter = nullptr;  // two device ints, zero before the launch and zero again after it: items are claimed
+                                // dynamically by the CTAs (nullptr: CTA c runs items c, c + grid, ...)
 };
 
 // Encode the tensor maps and launch the attention kernel; returns a CUDA error code (0 on success).

@@ -27,7 +27,9 @@ struct wa_plan {
   uint64_t lru = 0;
   wa::Item* d_items = nullptr;
   float* d_ws = nullptr;  // partial outputs followed by the log-sum-exp values
-  int* d_err = nullptr;
+  int* d_err = nullptr;       // the device error word, then two item counters of the attention kernel
+  int* d_counters = nullptr;  // = d_err + 1: two ints per counter; counter 0 for wa_forward, counters 0 and 1 for the
+                              // host path's two compute streams (launches on one stream are ordered)
   int64_t ws_o_elems = 0;
   cudaStream_t last_stream = nullptr;
   bool have_last = false;
@@ -340,7 +342,8 @@ wa_status create_uncached(const wa::Geometry& g, int dev, wa_plan** out) {
   p->ws_o_elems = (int64_t)g.layout.B * g.layout.H * g.G * p->hp.n_splits * g.layout.D;
   cudaError_t e = dev_alloc(&p->d_items, items_bytes);
   if (e == cudaSuccess && in.workspace_bytes > 0) e = dev_alloc(&p->d_ws, (size_t)in.workspace_bytes);
-  if (e == cudaSuccess) e = dev_alloc(&p->d_err, sizeof(int));
+  if (e == cudaSuccess) e = dev_alloc(&p->d_err, 5 * sizeof(int));
+  if (e == cudaSuccess) p->d_counters = p->d_err + 1;
   if (e != cudaSuccess) {
     cudaGetLastError();  // clear the sticky-free allocation error
     free_plan(p);
@@ -348,7 +351,7 @@ wa_status create_uncached(const wa::Geometry& g, int dev, wa_plan** out) {
   }
   if (cudaMemcpy(p->d_items, p->hp.items.data(), p->hp.items.size() * sizeof(wa::Item), cudaMemcpyHostToDevice) !=
           cudaSuccess ||
-      cudaMemset(p->d_err, 0, sizeof(int)) != cudaSuccess ||
+      cudaMemset(p->d_err, 0, 5 * sizeof(int)) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) != cudaSuccess) {
     free_plan(p);
     return WA_ERR_CUDA;
@@ -554,6 +557,7 @@ wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void
   a.qk_fp8 = qk_bytes == 1;
   a.qk_scale = qk_scale;
   a.lse = lse;
+  a.item_counter = plan->d_counters;
   cudaEvent_t* ev = nullptr;
   if (plan->profiling && plan->prof_n < kMaxProfiled) {
     while ((int)plan->prof_ev.size() < 3 * (plan->prof_n + 1)) {
@@ -785,6 +789,7 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
       return WA_ERR_CUDA;
     a.items = plan->d_items_pc + plan->pc_item_off[p];
     a.n_items = plan->pc_item_off[p + 1] - plan->pc_item_off[p];
+    a.item_counter = plan->d_counters + 2 * (p & 1);  // one per compute stream
     if (a.n_items > 0 && wa::launch_attention(a, (void*)cs, plan->num_sms) != 0) return WA_ERR_CUDA;
     if (plan->hs.out[p].empty()) continue;
     if (cudaEventRecord(ev_comp[p], cs) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_comp[p], 0) != cudaSuccess)

@@ -69,3 +69,21 @@ def test_static_scratch_rejects_oversized_geometry(cuda):
                                       ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(0))
     assert st == 2  # WA_ERR_UNSUPPORTED
     torch.cuda.synchronize()
+
+
+def test_dynamic_claiming_matches_static_striding(cuda):
+    """A plan's forward lets each CTA claim its next work item from a counter (the last CTA of a launch rewinds it);
+    wa_forward_static hands the same items out by static striding. Same items and the same arithmetic per item:
+    the results agree bit for bit, over several launches in a row on one plan (a counter left unrewound would make
+    the next launch skip its items and leave the NaN in place)."""
+    for w in (configs.MEDIUM, configs.RAGGED):
+        plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+        try:
+            for seed in (5, 6, 7):
+                q, k, v = inputs.make_qkv(w, seed=seed, device="cuda")
+                out = torch.full_like(q, float("nan"))
+                plan.forward(q, k, v, out=out)
+                assert plan.check_error() == 0
+                assert torch.equal(out, static_forward(cuda, w, q, k, v))
+        finally:
+            plan.close()
