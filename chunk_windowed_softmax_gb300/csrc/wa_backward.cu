@@ -48,6 +48,7 @@ struct BwdParams {
   float c_log2;       // log2(e) / sqrt(D): turns a raw score into log2 units of the scaled score
   float scale;        // 1 / sqrt(D)
   int debug_flags;
+  int* item_counter;  // ItemFeed counter (two ints, zero at launch); nullptr: static striding
 };
 
 // First row of the j-th 128-row tile of an item's segments, and how many of its rows belong to the segment.
@@ -103,11 +104,12 @@ __device__ __forceinline__ Smem align_smem(uint8_t* raw) {
   return Smem{s, smem_u32(s)};
 }
 
-// Every thread: wait for all roles, then warp 0 frees the tensor memory.
-__device__ __forceinline__ void teardown(uint32_t tmem, int warp) {
+// Every thread: wait for all roles, then warp 0 frees the tensor memory (and the CTA's item claims are over).
+__device__ __forceinline__ void teardown(uint32_t tmem, int warp, const ItemFeed& feed) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) feed.finish();
   if (warp == 0) {
     __syncwarp();  // tcgen05.dealloc is warp-collective: reconverge after the role branches
     tmem_dealloc(tmem, 512);
@@ -162,10 +164,11 @@ struct DqCfg {
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKSlots * kTileBytes;
   static constexpr int kBarOff = kVOff + kVSlots * kTileBytes;
-  // q_full, q_empty, s_full[2], p_full[2], dp_free, o_full, drain_x, drain_y, then the rings' full / empty barriers
-  static constexpr int kNumBars = 10 + 2 * kKSlots + 2 * kVSlots;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack of the dynamic window
+  // q_full, q_empty, s_full[2], p_full[2], dp_free, o_full, drain_x, drain_y, then the rings' full / empty barriers,
+  // then the work-item ring's (ItemFeed)
+  static constexpr int kNumBars = 10 + 2 * kKSlots + 2 * kVSlots + 2 * kItemRingSlots;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
+  static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kItemRingSlots + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
   static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 0, 1);   // dS from TMEM, key tile MN-major
@@ -219,6 +222,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto b_vempty = [&](uint32_t s) { return bar + 8 * (10 + 2 * C::kKSlots + C::kVSlots + s); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
+  const ItemFeed feed{prm.item_counter, prm.n_items, reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 16),
+                      bar + 8 * (C::kNumBars - 2 * kItemRingSlots)};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* err = prm.err;
 
@@ -233,6 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(b_ofull, 1);
     mbar_init(b_drain_x, 1);
     mbar_init(b_drain_y, 1);
+    feed.init(kEwWarps + 2);  // item consumers: issuers X and Y, the elementwise warps
     for (int s = 0; s < C::kKSlots; ++s) {
       mbar_init(b_kfull(s), 1);
       mbar_init(b_kempty(s), 1);
@@ -259,7 +265,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       uint32_t k_n = 0, v_n = 0, q_n = 0;
       bool ok = true, dropped = false;
-      for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+      for (uint32_t n = 0; ok; ++n) {
+        const int idx = feed.claim(n, abort_flag, err, ok);
+        if (idx < 0) break;
         const Item it = load_item(prm.items, idx);
         const int b = it.bh / prm.H, h = it.bh % prm.H;
         const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
@@ -322,7 +330,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss(d_tmem, a_lo + off, b_lo + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
-      for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+      for (uint32_t n = 0; ok; ++n) {
+        const int idx = feed.fetch(n, abort_flag, err, ok);
+        if (idx < 0) break;
         const Item it = load_item(prm.items, idx);
         const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
         const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
@@ -398,7 +408,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     uint32_t o_n = 0, gs = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+      const int idx = feed.fetch(n, abort_flag, err, ok);
+      if (idx < 0) break;
       const Item it = load_item(prm.items, idx);
       const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
       const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
@@ -456,7 +468,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   }
-  teardown(tmem, warp);
+  teardown(tmem, warp, feed);
 }
 
 // =====================================================================================================================
@@ -487,9 +499,9 @@ struct DkvCfg {
   static constexpr int kColBytes = 64 * 16;
   static constexpr int kBarOff = kColOff + kQSlots * kColBytes;
   // kv_full, kv_empty, s_full, p_full, dp_full, ds_full, o_full, drain_x, then q_full[slots], q_empty[slots]
-  static constexpr int kNumBars = 8 + 2 * kQSlots;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  static constexpr int kNumBars = 8 + 2 * kQSlots + 2 * kItemRingSlots;  // the last 2 kItemRingSlots: ItemFeed
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
+  static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kItemRingSlots + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
   static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 0, 1);  // A from TMEM, query-side tile MN-major
@@ -512,6 +524,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto b_qempty = [&](uint32_t s) { return bar + 8 * (8 + C::kQSlots + s); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
+  const ItemFeed feed{prm.item_counter, prm.n_items, reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 16),
+                      bar + 8 * (C::kNumBars - 2 * kItemRingSlots)};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* err = prm.err;
 
@@ -528,6 +542,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_qfull(s), 1 + 32);  // the copies' expect-tx arrival + one per loader lane (column values)
       mbar_init(b_qempty(s), 1 + kEwWarps);  // the MMA commit after dk(j) + one per elementwise warp
     }
+    feed.init(kEwWarps + 1);  // item consumers: the issuer, the elementwise warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -545,7 +560,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------------------------------------- loaders
     uint32_t kv_n = 0, q_n = 0;
     bool ok = true, dropped = false;
-    for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+      const int idx = feed.claim_warp(n, abort_flag, err, ok);
+      if (idx < 0) break;
       const Item it = load_item(prm.items, idx);
       const int b = it.bh / prm.H, h = it.bh % prm.H;
       const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
@@ -631,7 +648,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       auto slot_k = [&](uint32_t s, uint32_t tile) { return (uint32_t)dr_k + ((s * C::kSlotBytes + tile) >> 4); };
       auto slot_mn = [&](uint32_t s, uint32_t tile) { return (uint32_t)dr_mn + ((s * C::kSlotBytes + tile) >> 4); };
-      for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+      for (uint32_t n = 0; ok; ++n) {
+        const int idx = feed.fetch(n, abort_flag, err, ok);
+        if (idx < 0) break;
         const Item it = load_item(prm.items, idx);
         const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
         const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
@@ -691,7 +710,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     uint32_t q_n = 0, s_n = 0, o_n = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < prm.n_items && ok; idx += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+      const int idx = feed.fetch(n, abort_flag, err, ok);
+      if (idx < 0) break;
       const Item it = load_item(prm.items, idx);
       const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
       const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
@@ -783,7 +804,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   }
-  teardown(tmem, warp);
+  teardown(tmem, warp, feed);
 }
 
 // Dvec_i = dout_i . out_i for every (b, i, h), one warp per row, rows in memory order; fp32 into [B*H][L].
@@ -898,6 +919,7 @@ int launch_backward_d(const BackwardArgs& a, cudaStream_t s, int num_sms, void* 
   p.c_log2 = (float)(1.4426950408889634 / sqrt((double)D));
   p.scale = (float)(1.0 / sqrt((double)D));
   p.debug_flags = a.debug_flags;
+  p.item_counter = a.item_counter;
   const int grid = a.n_items < num_sms ? a.n_items : num_sms;
   if (grid > 0) {
     wa_dq_kernel<D><<<grid, kBwdThreads, DqCfg<D>::kSmemBytes, s>>>(mq, mk, mv, mdo, p);

@@ -1,10 +1,12 @@
-// Device helpers shared by the forward and backward kernels: the work-item view, wait limits and bf16 packing.
+// Device helpers shared by the forward and backward kernels: the work-item view and its hand-out to the CTAs of
+// a persistent launch, wait limits and bf16 packing.
 #pragma once
 
 #include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "wa_internal.h"
+#include "wa_ptx.cuh"
 
 namespace wa {
 
@@ -20,6 +22,82 @@ __device__ __forceinline__ Item load_item(const Item* items, int idx) {
 
 // Number of 128-row tiles of the half-open row range [lo, hi).
 __device__ __forceinline__ int seg_tiles(int lo, int hi) { return hi > lo ? (hi - lo + kTileRows - 1) / kTileRows : 0; }
+
+// Hand-out of the work items of a persistent launch to its CTAs. Without a counter, CTA c runs the items c,
+// c + grid, c + 2 grid, ... With a counter (two device ints, zero when the launch starts: items claimed so far and
+// CTAs finished), one producer thread of each CTA claims the next unclaimed item when it is ready for one, so CTAs
+// that run faster take more items and all of them finish within about one item of each other; it passes the index
+// to the CTA's consuming warps through a ring of kItemRingSlots shared-memory slots, each guarded by a "full"
+// mbarrier (the index is written) and an "empty" one (every consuming warp has read it). The last CTA to finish
+// sets the counter back to zero for the next launch. Every wait is bounded.
+constexpr int kItemRingSlots = 4;
+
+struct ItemFeed {
+  int* counter;         // nullptr: static striding
+  int n_items;
+  volatile int* ring;   // kItemRingSlots ints of shared memory
+  uint32_t bars;        // 2 * kItemRingSlots mbarriers (8 bytes each): full[kItemRingSlots], then empty[...]
+
+  __device__ __forceinline__ bool dynamic() const { return counter != nullptr; }
+  __device__ __forceinline__ uint32_t full(uint32_t n) const { return bars + 8 * (n % kItemRingSlots); }
+  __device__ __forceinline__ uint32_t empty(uint32_t n) const {
+    return bars + 8 * (kItemRingSlots + n % kItemRingSlots);
+  }
+  __device__ __forceinline__ int static_item(uint32_t n) const {
+    const int64_t i = blockIdx.x + (int64_t)n * gridDim.x;
+    return i < n_items ? (int)i : -1;
+  }
+  // One thread, before the CTA's first barrier sync: `consumers` warps read every index.
+  __device__ __forceinline__ void init(int consumers) const {
+    for (int s = 0; s < kItemRingSlots; ++s) {
+      ptx::mbar_init(full(s), 1);
+      ptx::mbar_init(empty(s), consumers);
+    }
+  }
+  // The producer thread: the item of its n-th iteration, or -1 when there are no more (or on an error: ok = false).
+  __device__ __forceinline__ int claim(uint32_t n, volatile int* abort_flag, int* err, bool& ok) const {
+    if (!dynamic()) return static_item(n);
+    if (n >= (uint32_t)kItemRingSlots) {  // the slot's previous index must have been read by every consumer
+      const uint32_t w = n - kItemRingSlots;
+      ok = ptx::mbar_wait(empty(w), (w / kItemRingSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+      if (!ok) return -1;
+    }
+    int i = atomicAdd(counter, 1);
+    if (i >= n_items) i = -1;
+    ring[n % kItemRingSlots] = i;
+    ptx::mbar_arrive(full(n));  // release: the index is visible to whoever completes the wait
+    return i;
+  }
+  // claim() for a producer that is a whole warp: lane 0 claims, every lane gets the index and the outcome.
+  __device__ __forceinline__ int claim_warp(uint32_t n, volatile int* abort_flag, int* err, bool& ok) const {
+    int i = -1;
+    bool good = true;
+    if ((threadIdx.x & 31) == 0) i = claim(n, abort_flag, err, good);
+    i = __shfl_sync(0xffffffffu, i, 0);
+    if (!__shfl_sync(0xffffffffu, (int)good, 0)) ok = false;
+    return i;
+  }
+  // A whole consuming warp: the same item as the producer's n-th iteration, or -1 (ok = false on an error).
+  __device__ __forceinline__ int fetch(uint32_t n, volatile int* abort_flag, int* err, bool& ok) const {
+    if (!dynamic()) return static_item(n);
+    ok = ptx::mbar_wait(full(n), (n / kItemRingSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return -1;
+    const int i = ring[n % kItemRingSlots];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(empty(n));
+    return i;
+  }
+  // One thread per CTA, once every role of the CTA is done: the last CTA out rewinds the counter.
+  __device__ __forceinline__ void finish() const {
+    if (!dynamic()) return;
+    __threadfence();
+    if (atomicAdd(counter + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(counter, 0);
+      atomicExch(counter + 1, 0);
+    }
+  }
+};
 
 // Two fp32 values rounded to nearest-even bf16 and packed low-first into 32 bits.
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {

@@ -103,6 +103,7 @@ struct BackwardArgs {
   int n_splits;
   int debug_flags;
   const Geometry* geo;
+  int* item_counter = nullptr;  // as LaunchArgs::item_counter, shared by the dq and dk/dv launches (stream-ordered)
 };
 
 // Launch the backward (row dot products, dq kernel, dk/dv kernel, split sums) on `stream`. `events`, when not null,

@@ -51,10 +51,7 @@ constexpr uint32_t kSoftmaxRegs = 192;
 constexpr uint32_t kControlRegs = 120;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split exceeds the launch");
 constexpr float kLazyLimit = 65536.0f;  // a step's row sum above this (relative to the reference m) raises m
-// Dynamic item claiming: the producer claims item indices from a global counter and hands them to the consuming
-// warps (the MMA warp and the 8 softmax warps) through a ring of kIdxSlots shared-memory slots.
-constexpr int kIdxSlots = 4;
-constexpr int kIdxConsumers = 9;
+constexpr int kItemConsumers = 9;  // warps that take every work item from the producer: the MMA warp, 8 softmax
 
 // kF8: q and k are e4m3 (one byte per element) and the scores use kind::f8f6f4 MMAs; v, P and O stay bf16 / fp32.
 template <int D, bool kF8>
@@ -80,10 +77,10 @@ struct Cfg {
   static constexpr int kVOff = kKOff + kKSlots * kQTileBytes;
   static constexpr int kBarOff = kVOff + kVSlots * kVTileBytes;
   // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain b_full[kLag] b_empty[kLag]
-  //           idx_full[kIdxSlots] idx_empty[kIdxSlots]
-  static constexpr int kNumBars = 11 + 2 * kLag + 2 * kIdxSlots;
+  //           item ring full[kItemRingSlots] empty[kItemRingSlots]
+  static constexpr int kNumBars = 11 + 2 * kLag + 2 * kItemRingSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
-  static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kIdxSlots + 1024;  // + slack for 1024-byte alignment
+  static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kItemRingSlots + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t kTmemO = 256;
   static constexpr uint32_t kIdescS = kF8 ? idesc_e4m3_f32(128, 128)
                                          : idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
@@ -104,9 +101,7 @@ struct Params {
   int debug_flags;
   float* lse;     // optional [B][H][L] row log-sum-exp output (natural log); nullptr when not wanted
   int L;
-  // Two ints, zero at launch: items claimed so far, CTAs finished. Items are claimed dynamically and the last CTA
-  // to finish sets both back to zero for the next launch. nullptr: static striding.
-  int* item_counter;
+  int* item_counter;  // ItemFeed counter (two ints, zero at launch); nullptr: static striding
 };
 
 // Shared-memory barrier layout, relative to the barrier block: q_full[2] q_empty[2] s_full[2] p_full[2]
@@ -124,11 +119,8 @@ struct BarAddr {
   // bundle b: full (copies landed) and empty (the MMAs reading it completed)
   __device__ __forceinline__ uint32_t b_full(uint32_t b) const { return base + 8 * (11 + b % NB); }
   __device__ __forceinline__ uint32_t b_empty(uint32_t b) const { return base + 8 * (11 + NB + b % NB); }
-  // item ring slot of the n-th item: full (index written) and empty (every consumer read it)
-  __device__ __forceinline__ uint32_t idx_full(uint32_t n) const { return base + 8 * (11 + 2 * NB + n % kIdxSlots); }
-  __device__ __forceinline__ uint32_t idx_empty(uint32_t n) const {
-    return base + 8 * (11 + 2 * NB + kIdxSlots + n % kIdxSlots);
-  }
+  // the work-item ring's barriers (ItemFeed)
+  __device__ __forceinline__ uint32_t item_ring() const { return base + 8 * (11 + 2 * NB); }
 };
 
 // Exponentiate one 128-column score row into bf16 P (written to TMEM over the row's S columns, 16 columns per
@@ -166,9 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = s_base + C::kBarOff;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
-  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 16);
 
   const BarAddr<C::kLag> bars{bar0};
+  const ItemFeed feed{prm.item_counter, prm.n_items, reinterpret_cast<volatile int*>(smem + C::kMiscOff + 16),
+                      bars.item_ring()};
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -188,10 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.b_full(s), 1);
       mbar_init(bars.b_empty(s), 1);
     }
-    for (int s = 0; s < kIdxSlots; ++s) {
-      mbar_init(bars.idx_full(s), 1);
-      mbar_init(bars.idx_empty(s), kIdxConsumers);  // one arrive per consuming warp
-    }
+    feed.init(kItemConsumers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -210,49 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   int* err = prm.err;
 
-  // The item of a role's n-th loop iteration, or -1 when there is none. Static striding gives CTA c the items
-  // c, c + grid, ...; with a counter, the producer claims the next unclaimed item when it is ready for one (so CTAs
-  // that run faster take more items and all finish within about one item of each other) and passes the index on.
-  const bool dyn = prm.item_counter != nullptr;
-  auto static_item = [&](uint32_t n) {
-    const int64_t i = blockIdx.x + (int64_t)n * gridDim.x;
-    return i < prm.n_items ? (int)i : -1;
-  };
-  auto claim_item = [&](uint32_t n, bool& ok) -> int {  // the producer thread
-    if (!dyn) return static_item(n);
-    if (n >= (uint32_t)kIdxSlots) {  // the slot's previous index must have been read by every consumer
-      const uint32_t w = n - kIdxSlots;
-      ok = mbar_wait(bars.idx_empty(w), (w / kIdxSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-      if (!ok) return -1;
-    }
-    int i = atomicAdd(prm.item_counter, 1);
-    if (i >= prm.n_items) i = -1;
-    item_ring[n % kIdxSlots] = i;
-    mbar_arrive(bars.idx_full(n));  // release: the index is visible to whoever completes the wait
-    return i;
-  };
-  auto fetch_item = [&](uint32_t n, bool& ok) -> int {  // a whole consuming warp
-    if (!dyn) return static_item(n);
-    ok = mbar_wait(bars.idx_full(n), (n / kIdxSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) return -1;
-    const int i = item_ring[n % kIdxSlots];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars.idx_empty(n));
-    return i;
-  };
-
   auto teardown = [&]() {  // every thread: wait for all roles, then warp 0 frees the tensor memory
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (dyn && tid == 0) {  // this CTA's claims are over; the last CTA out rewinds the counter for the next launch
-      __threadfence();
-      if (atomicAdd(prm.item_counter + 1, 1) == (int)gridDim.x - 1) {
-        atomicExch(prm.item_counter, 0);
-        atomicExch(prm.item_counter + 1, 0);
-      }
-    }
+    if (tid == 0) feed.finish();  // this CTA's claims are over (the last CTA out rewinds the counter)
     if (warp == 0) {
       __syncwarp();  // tcgen05.dealloc is warp-collective: reconverge after the role branches
       tmem_dealloc(tmem, 512);
@@ -269,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool dropped = false;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n) {
-        const int idx = claim_item(n, ok);
+        const int idx = feed.claim(n, abort_flag, err, ok);
         if (idx < 0) break;
         const Item it = load_item(prm.items, idx);
         const int b = it.bh / prm.H, h = it.bh % prm.H;
@@ -366,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       for (uint32_t n = 0; ok; ++n) {
-        const int idx = fetch_item(n, ok);
+        const int idx = feed.fetch(n, abort_flag, err, ok);
         if (idx < 0) break;
         const Item it = load_item(prm.items, idx);
         const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
@@ -431,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t s_n = 0, o_n = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
-      const int idx = fetch_item(n, ok);  // every softmax warp takes every item (and releases its ring slot)
+      const int idx = feed.fetch(n, abort_flag, err, ok);  // every softmax warp takes every item
       if (idx < 0) break;
       const Item it = load_item(prm.items, idx);
       const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;

@@ -655,6 +655,7 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
   a.n_splits = plan->hp.n_splits;
   a.debug_flags = plan->debug_flags;
   a.geo = &g;
+  a.item_counter = plan->d_counters;
   void* const* ev = nullptr;
   if (plan->profiling && plan->bprof_n < kMaxProfiled) {
     while ((int)plan->bprof_ev.size() < 5 * (plan->bprof_n + 1)) {
