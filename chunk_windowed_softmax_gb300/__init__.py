@@ -190,23 +190,24 @@ def wa_geometry_describe(T, S, K, r, G, layout, with_groups=True, with_items=Fal
 
 
 def wa_host_schedule_describe(T, S, K, r, G, layout, n_items):
-    """Host-only piece schedule of the host-buffer forward: {"row_pieces": bool, "pieces": [(lo, hi)] in copy order,
-    "item_launch": [launch per work item, in wa_geometry_describe's item order], "out": [(launch, lo, hi)]}."""
+    """Host-only piece schedule of the host-buffer forward: {"row_pieces": bool, "pieces": [(lo, hi, h_lo, h_hi)] in
+    copy order, "item_launch": [launch per work item, in wa_geometry_describe's item order],
+    "out": [(launch, lo, hi, h_lo, h_hi)]}."""
     L = lib()
     n_pieces, n_out, rows = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
     args = (T, S, K, r, G, ctypes.byref(layout))
     _check(L.wa_host_schedule_describe(*args, None, 0, None, 0, None, 0, ctypes.byref(n_pieces), ctypes.byref(n_out),
                                        ctypes.byref(rows)), "wa_host_schedule_describe")
-    pbuf = (ctypes.c_int64 * (2 * max(1, n_pieces.value)))()
+    pbuf = (ctypes.c_int64 * (4 * max(1, n_pieces.value)))()
     lbuf = (ctypes.c_int32 * max(1, n_items))()
-    obuf = (ctypes.c_int64 * (3 * max(1, n_out.value)))()
+    obuf = (ctypes.c_int64 * (5 * max(1, n_out.value)))()
     _check(L.wa_host_schedule_describe(*args, pbuf, n_pieces.value, lbuf, n_items, obuf, n_out.value,
                                        ctypes.byref(n_pieces), ctypes.byref(n_out), ctypes.byref(rows)),
            "wa_host_schedule_describe")
     return {"row_pieces": bool(rows.value),
-            "pieces": [(pbuf[2 * i], pbuf[2 * i + 1]) for i in range(n_pieces.value)],
+            "pieces": [tuple(pbuf[4 * i:4 * i + 4]) for i in range(n_pieces.value)],
             "item_launch": list(lbuf[:n_items]),
-            "out": [tuple(obuf[3 * i:3 * i + 3]) for i in range(n_out.value)]}
+            "out": [tuple(obuf[5 * i:5 * i + 5]) for i in range(n_out.value)]}
 
 
 # ----------------------------------------------------------------------------------------- torch side

@@ -39,13 +39,20 @@ struct HostPlan {
   int n_splits;
 };
 
-// The piece schedule of the host-buffer forward: the sequence rows copied in, piece by piece, and after piece p
-// launch p of the items whose rows have all arrived; after launch p the rows of out it completed are copied back.
+// The piece schedule of the host-buffer forward: blocks of sequence rows x heads (all batch entries) copied in one
+// after the other; after piece p, launch p of the items whose rows have all arrived; after launch p, the blocks of
+// out it completed are copied back.
+struct HostBlock {
+  int64_t lo, hi;  // sequence rows [lo, hi)
+  int h_lo, h_hi;  // heads [h_lo, h_hi)
+};
 struct HostSchedule {
-  bool rows = false;                    // pieces are row blocks of all heads (else one piece: the whole tensors)
-  std::vector<int64_t> lo, hi;          // piece p: sequence rows [lo[p], hi[p]) of every batch entry, in copy order
-  std::vector<int> launch;              // per item of HostPlan::items (same order): the launch that runs it
-  std::vector<std::vector<std::pair<int64_t, int64_t>>> out;  // per launch: frame rows of out it completes
+  bool rows = false;                         // pieces are row blocks (else one piece: the whole tensors)
+  std::vector<HostBlock> pieces;             // in copy order
+  std::vector<int> launch;                   // per item of HostPlan::items (same order): the launch that runs it
+  std::vector<std::vector<HostBlock>> out;    // per launch: the blocks of out (frame rows) it completes
+  std::vector<std::vector<HostBlock>> merge;  // per launch: global-row blocks whose heads' split items are all done
+                                              // after it (merged, then copied back, right behind it)
 };
 
 // Validate arguments; on success fill `geo`.

@@ -187,6 +187,9 @@ void build_host_plan(const Geometry& g, HostPlan* hp) {
 // At most this many pieces (and launches) per host-buffer forward; geometries with more window groups merge
 // neighbouring pieces.
 constexpr int kMaxPieces = 64;
+// Head ranges of the first pieces (the globals and the first window group's rows) and of the last frame piece.
+constexpr int kStartHeadSplits = 2;
+constexpr int kEndHeadSplits = 4;
 
 // One past the last sequence row that the attention kernel reads for the row range [lo, hi): it reads whole 128-row
 // tiles from the start of the range, so the last tile also reads rows past its end (rows past L read as zeros).
@@ -198,23 +201,23 @@ static int64_t read_end(const Geometry& g, int64_t lo, int64_t hi) {
 void build_host_schedule(const HostPlan& hp, HostSchedule* hs) {
   const Geometry& g = hp.geo;
   const wa_layout_t& l = g.layout;
-  // With the heads of a row adjacent (stride_h == D), a range of sequence rows of one batch entry is one strided
-  // 2-D block, copied at full speed. Otherwise the tensors are copied whole as one piece.
-  hs->rows = l.H == 1 || l.stride_h == l.D;
-  hs->lo.clear();
-  hs->hi.clear();
+  const int H = l.H;
+  // With the heads of a row adjacent (stride_h == D), a block of sequence rows x consecutive heads of one batch
+  // entry is one strided 2-D copy at full speed. Otherwise the tensors are copied whole as one piece.
+  hs->rows = H == 1 || l.stride_h == l.D;
+  hs->pieces.clear();
   if (!hs->rows) {
-    hs->lo.push_back(0);
-    hs->hi.push_back(g.L);
+    hs->pieces.push_back({0, g.L, 0, H});
   } else {
     // The globals first (every window item reads them), then the frames in order, cut where a window group's reads
     // end: each group can start as soon as the piece holding its last row has arrived. Measured at 56 heads x
     // 99,968 rows (34 groups of one chunk; a row block copies at the full 211 GB/s host-to-device rate): 24.2 ms
     // with one chunk per piece, 24.5 with two, 25.4 with four; head groups copied as strided blocks took 27.4 ms.
-    if (g.G > 0) {
-      hs->lo.push_back(g.g0);
-      hs->hi.push_back(g.g0 + g.G);
-    }
+    // The first launch waits for the globals and the first group's rows; to start it sooner, those two pieces
+    // are split into kStartHeadSplits head ranges, so that the first group's first heads start after a fraction
+    // of that copy. The copies set the pace (4.3 GB in at 211 GB/s, slowed by the copies out), so what matters
+    // most is the work left after the last byte arrives: the last frame piece is split into kEndHeadSplits head
+    // ranges, and each range's global rows are merged and copied back as soon as its last launch is done.
     const int64_t f_lo = g.f0, f_hi = g.f0 + g.F;
     // The last frame row read for [lo, hi), plus one (f_lo when the reads hold no frame row, e.g. the globals).
     auto frame_end = [&](int64_t lo, int64_t hi) {
@@ -229,50 +232,97 @@ void build_host_schedule(const HostPlan& hp, HostSchedule* hs) {
       if (cuts.empty() || end > cuts.back()) cuts.push_back(end);
     }
     if (cuts.empty() || cuts.back() != f_hi) cuts.push_back(f_hi);
-    const int max_frame_pieces = kMaxPieces - (g.G > 0 ? 1 : 0);
+    const int splits = std::min(H, kStartHeadSplits), end_splits = std::min(H, kEndHeadSplits);
+    const int start_pieces = splits * (g.G > 0 ? 2 : 1);
+    const int max_frame_pieces = kMaxPieces - start_pieces - end_splits + 2;
     const int n_cuts = (int)cuts.size();
+    std::vector<std::pair<int64_t, int64_t>> frames;
     int64_t lo = f_lo;
     for (int i = 0; i < std::min(n_cuts, max_frame_pieces); ++i) {
       // every cut when they fit, else evenly spaced ones (always including the last)
       const int64_t hi =
           n_cuts <= max_frame_pieces ? cuts[i] : cuts[(int64_t)(i + 1) * n_cuts / max_frame_pieces - 1];
-      hs->lo.push_back(lo);
-      hs->hi.push_back(hi);
+      frames.emplace_back(lo, hi);
       lo = hi;
     }
+    for (int s = 0; s < splits; ++s) {
+      const int h_lo = (int)((int64_t)H * s / splits), h_hi = (int)((int64_t)H * (s + 1) / splits);
+      if (g.G > 0) hs->pieces.push_back({g.g0, g.g0 + g.G, h_lo, h_hi});
+      hs->pieces.push_back({frames[0].first, frames[0].second, h_lo, h_hi});
+    }
+    for (size_t i = 1; i < frames.size(); ++i) {
+      if (i + 1 < frames.size()) {
+        hs->pieces.push_back({frames[i].first, frames[i].second, 0, H});
+        continue;
+      }
+      for (int s = 0; s < end_splits; ++s)
+        hs->pieces.push_back({frames[i].first, frames[i].second, (int)((int64_t)H * s / end_splits),
+                              (int)((int64_t)H * (s + 1) / end_splits)});
+    }
   }
-  const int n_pieces = (int)hs->lo.size();
-  // The launch of an item: the latest piece among those holding a row it reads.
-  auto last_piece = [&](int64_t lo, int64_t hi) {
+  const int n_pieces = (int)hs->pieces.size();
+  // The launch of an item: the latest piece among those holding a row it reads, for the item's head.
+  auto last_piece = [&](int h, int64_t lo, int64_t hi) {
     int last = 0;
     if (hi <= lo) return last;
     hi = read_end(g, lo, hi);
-    for (int p = 0; p < n_pieces; ++p)
-      if (hs->lo[p] < hi && lo < hs->hi[p]) last = p;
+    for (int p = 0; p < n_pieces; ++p) {
+      const HostBlock& pc = hs->pieces[p];
+      if (pc.h_lo <= h && h < pc.h_hi && pc.lo < hi && lo < pc.hi) last = p;
+    }
     return last;
   };
   auto launch_of = [&](const Item& it) {
-    return std::max({last_piece(it.q_lo, it.q_hi), last_piece(it.s0_lo, it.s0_hi), last_piece(it.s1_lo, it.s1_hi)});
+    const int h = it.bh % H;
+    return std::max({last_piece(h, it.q_lo, it.q_hi), last_piece(h, it.s0_lo, it.s0_hi),
+                     last_piece(h, it.s1_lo, it.s1_hi)});
   };
   hs->launch.resize(hp.items.size());
   for (size_t i = 0; i < hp.items.size(); ++i) hs->launch[i] = launch_of(hp.items[i]);
-  // A window group's rows of out are complete after the launch of its items (the same launch for all of them: they
-  // read the same rows). Adjacent groups finished by one launch are copied back as one range. Without row pieces
-  // the whole of out is copied back at the end instead.
+  // A window group's rows of out, for one head, are complete after the launch of the group's items of that head
+  // (the same launch for all of them: they read the same rows). Runs of heads finished by the same launch form one
+  // block; blocks of adjacent groups with the same heads and launch are merged. Without row pieces the whole of out
+  // is copied back at the end instead.
   hs->out.assign(n_pieces, {});
   if (hs->rows) {
+    std::vector<int> head_launch(H);
     for (const wa_group_t& gr : hp.groups) {
-      int launch = 0;
-      for (int64_t q = gr.q_lo; q < gr.q_hi; q += kItemRows) {
-        const Item it{0, -1, (int32_t)q, (int32_t)std::min<int64_t>(gr.q_hi, q + kItemRows), (int32_t)gr.kv0_lo,
-                      (int32_t)gr.kv0_hi, (int32_t)gr.kv1_lo, (int32_t)gr.kv1_hi};
-        launch = std::max(launch, launch_of(it));
+      for (int h = 0; h < H; ++h) {
+        int launch = 0;
+        for (int64_t q = gr.q_lo; q < gr.q_hi; q += kItemRows) {
+          const Item it{h, -1, (int32_t)q, (int32_t)std::min<int64_t>(gr.q_hi, q + kItemRows), (int32_t)gr.kv0_lo,
+                        (int32_t)gr.kv0_hi, (int32_t)gr.kv1_lo, (int32_t)gr.kv1_hi};
+          launch = std::max(launch, launch_of(it));
+        }
+        head_launch[h] = launch;
       }
-      auto& ranges = hs->out[launch];
-      if (!ranges.empty() && ranges.back().second == gr.q_lo)
-        ranges.back().second = gr.q_hi;
-      else
-        ranges.emplace_back(gr.q_lo, gr.q_hi);
+      for (int h0 = 0; h0 < H;) {
+        int h1 = h0 + 1;
+        while (h1 < H && head_launch[h1] == head_launch[h0]) ++h1;
+        auto& blocks = hs->out[head_launch[h0]];
+        if (!blocks.empty() && blocks.back().hi == gr.q_lo && blocks.back().h_lo == h0 && blocks.back().h_hi == h1)
+          blocks.back().hi = gr.q_hi;
+        else
+          blocks.push_back({gr.q_lo, gr.q_hi, h0, h1});
+        h0 = h1;
+      }
+    }
+  }
+  // The global rows of a head can be merged once its last split item has run: runs of heads whose last split item
+  // is in the same launch form one merge block of that launch. Without row pieces everything is merged at the end.
+  hs->merge.assign(n_pieces, {});
+  if (hs->rows && g.G > 0) {
+    std::vector<int> head_last(H, 0);
+    for (size_t i = 0; i < hp.items.size(); ++i)
+      if (hp.items[i].split >= 0) {
+        const int h = hp.items[i].bh % H;
+        head_last[h] = std::max(head_last[h], hs->launch[i]);
+      }
+    for (int h0 = 0; h0 < H;) {
+      int h1 = h0 + 1;
+      while (h1 < H && head_last[h1] == head_last[h0]) ++h1;
+      hs->merge[head_last[h0]].push_back({g.g0, g.g0 + g.G, h0, h1});
+      h0 = h1;
     }
   }
 }
@@ -420,25 +470,26 @@ wa_status wa_host_schedule_describe(int T, int S, int K, int r, int G, const wa_
   wa::build_host_plan(g, &hp);
   wa::HostSchedule hs;
   wa::build_host_schedule(hp, &hs);
-  *n_pieces = (int64_t)hs.lo.size();
+  *n_pieces = (int64_t)hs.pieces.size();
   *row_pieces = hs.rows ? 1 : 0;
   if (pieces)
     for (int64_t i = 0; i < std::min<int64_t>(pieces_cap, *n_pieces); ++i) {
-      pieces[2 * i] = hs.lo[i];
-      pieces[2 * i + 1] = hs.hi[i];
+      const wa::HostBlock& pc = hs.pieces[i];
+      int64_t* o = pieces + 4 * i;
+      o[0] = pc.lo; o[1] = pc.hi; o[2] = pc.h_lo; o[3] = pc.h_hi;
     }
   if (item_launch)
     for (int64_t i = 0; i < std::min<int64_t>(items_cap, (int64_t)hs.launch.size()); ++i) item_launch[i] = hs.launch[i];
   int64_t n = 0;
   for (size_t p = 0; p < hs.out.size(); ++p)
-    for (const auto& range : hs.out[p]) {
-      if (out_ranges && n < out_cap) {
-        out_ranges[3 * n] = (int64_t)p;
-        out_ranges[3 * n + 1] = range.first;
-        out_ranges[3 * n + 2] = range.second;
+    for (const auto* list : {&hs.out[p], &hs.merge[p]})
+      for (const wa::HostBlock& blk : *list) {
+        if (out_ranges && n < out_cap) {
+          int64_t* o = out_ranges + 5 * n;
+          o[0] = (int64_t)p; o[1] = blk.lo; o[2] = blk.hi; o[3] = blk.h_lo; o[4] = blk.h_hi;
+        }
+        ++n;
       }
-      ++n;
-    }
   *n_out = n;
   return WA_OK;
 }
@@ -678,7 +729,7 @@ namespace {
 wa_status prepare_host_path(wa_plan_t* plan, size_t span_bytes) {
   if (plan->d_stage) return WA_OK;
   wa::build_host_schedule(plan->hp, &plan->hs);
-  const int n_pieces = (int)plan->hs.lo.size();
+  const int n_pieces = (int)plan->hs.pieces.size();
   std::vector<std::vector<wa::Item>> by_launch(n_pieces);
   for (size_t i = 0; i < plan->hp.items.size(); ++i)  // keeps the longest-first order inside each launch
     by_launch[plan->hs.launch[i]].push_back(plan->hp.items[i]);
@@ -705,22 +756,23 @@ wa_status prepare_host_path(wa_plan_t* plan, size_t span_bytes) {
       cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&plan->s_c2, cudaStreamNonBlocking) != cudaSuccess)
     return WA_ERR_CUDA;
-  plan->pc_ev.resize(2 * n_pieces + 4);
+  plan->pc_ev.resize(3 * n_pieces + 4);
   for (cudaEvent_t& ev : plan->pc_ev)
     if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return WA_ERR_CUDA;
   return WA_OK;
 }
 
-// Copy sequence rows [lo, hi) of every batch entry (all heads) between two buffers of the plan's layout.
-cudaError_t copy_rows(const wa::Geometry& g, void* dst, const void* src, int64_t lo, int64_t hi, cudaMemcpyKind kind,
-                      cudaStream_t st) {
+// Copy one block (sequence rows [lo, hi) x heads [h_lo, h_hi) of every batch entry) between two buffers of the
+// plan's layout: one strided 2-D copy per batch entry.
+cudaError_t copy_block(const wa::Geometry& g, void* dst, const void* src, const wa::HostBlock& blk,
+                       cudaMemcpyKind kind, cudaStream_t st) {
   const wa_layout_t& l = g.layout;
-  const size_t width = (size_t)((l.H - 1) * l.stride_h + l.D) * 2;
+  const size_t width = (size_t)((blk.h_hi - blk.h_lo - 1) * l.stride_h + l.D) * 2;
   const size_t pitch = std::max<size_t>((size_t)l.stride_l * 2, width);
   for (int b = 0; b < l.B; ++b) {
-    const size_t off = (size_t)(b * l.stride_b + lo * l.stride_l) * 2;
+    const size_t off = (size_t)(b * l.stride_b + blk.lo * l.stride_l + (int64_t)blk.h_lo * l.stride_h) * 2;
     cudaError_t e = cudaMemcpy2DAsync((uint8_t*)dst + off, pitch, (const uint8_t*)src + off, pitch, width,
-                                      (size_t)(hi - lo), kind, st);
+                                      (size_t)(blk.hi - blk.lo), kind, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -756,11 +808,12 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
   uint8_t* dk = dq + stage_span;
   uint8_t* dv = dk + stage_span;
   uint8_t* dout = dv + stage_span;
-  const int n_pieces = (int)plan->hs.lo.size();
-  cudaEvent_t* ev_in = &plan->pc_ev[0];
-  cudaEvent_t* ev_comp = &plan->pc_ev[n_pieces];
-  cudaEvent_t ev_start = plan->pc_ev[2 * n_pieces], ev_c2 = plan->pc_ev[2 * n_pieces + 1];
-  cudaEvent_t ev_merged = plan->pc_ev[2 * n_pieces + 2], ev_outdone = plan->pc_ev[2 * n_pieces + 3];
+  const int n_pieces = (int)plan->hs.pieces.size();
+  cudaEvent_t* ev_in = &plan->pc_ev[0];                // piece p copied in
+  cudaEvent_t* ev_comp = &plan->pc_ev[n_pieces];       // launch p done
+  cudaEvent_t* ev_post = &plan->pc_ev[2 * n_pieces];   // launch p and its merges done
+  cudaEvent_t ev_start = plan->pc_ev[3 * n_pieces], ev_c2 = plan->pc_ev[3 * n_pieces + 1];
+  cudaEvent_t ev_merged = plan->pc_ev[3 * n_pieces + 2], ev_outdone = plan->pc_ev[3 * n_pieces + 3];
   // The helper streams start behind everything already queued on the caller's stream (earlier users of the staging).
   if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(plan->s_in, ev_start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(plan->s_out, ev_start, 0) != cudaSuccess ||
@@ -779,8 +832,7 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
   for (int p = 0; p < n_pieces; ++p) {
     for (int x = 0; x < 3; ++x) {
       cudaError_t e = plan->hs.rows
-                          ? copy_rows(g, dst[x], src[x], plan->hs.lo[p], plan->hs.hi[p], cudaMemcpyHostToDevice,
-                                      plan->s_in)
+                          ? copy_block(g, dst[x], src[x], plan->hs.pieces[p], cudaMemcpyHostToDevice, plan->s_in)
                           : cudaMemcpyAsync(dst[x], src[x], span, cudaMemcpyHostToDevice, plan->s_in);
       if (e != cudaSuccess) return WA_ERR_CUDA;
     }
@@ -792,25 +844,36 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
     a.n_items = plan->pc_item_off[p + 1] - plan->pc_item_off[p];
     a.item_counter = plan->d_counters + 2 * (p & 1);  // one per compute stream
     if (a.n_items > 0 && wa::launch_attention(a, (void*)cs, plan->num_sms) != 0) return WA_ERR_CUDA;
-    if (plan->hs.out[p].empty()) continue;
-    if (cudaEventRecord(ev_comp[p], cs) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_comp[p], 0) != cudaSuccess)
+    if (cudaEventRecord(ev_comp[p], cs) != cudaSuccess) return WA_ERR_CUDA;
+    const auto& merges = plan->hs.merge[p];
+    if (!merges.empty()) {
+      // The heads' earlier split items may have run in the other stream's launches: wait for its latest one.
+      if (p >= 1 && cudaStreamWaitEvent(cs, ev_comp[p - 1], 0) != cudaSuccess) return WA_ERR_CUDA;
+      for (const wa::HostBlock& blk : merges) {
+        a.head_first = blk.h_lo;
+        a.head_count = blk.h_hi - blk.h_lo;
+        if (wa::launch_combine(a, (void*)cs) != 0) return WA_ERR_CUDA;
+      }
+    }
+    if (plan->hs.out[p].empty() && merges.empty()) continue;
+    if (cudaEventRecord(ev_post[p], cs) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_post[p], 0) != cudaSuccess)
       return WA_ERR_CUDA;
-    for (const auto& range : plan->hs.out[p])
-      if (copy_rows(g, out, dout, range.first, range.second, cudaMemcpyDeviceToHost, plan->s_out) != cudaSuccess)
-        return WA_ERR_CUDA;
+    for (const wa::HostBlock& blk : plan->hs.out[p])
+      if (copy_block(g, out, dout, blk, cudaMemcpyDeviceToHost, plan->s_out) != cudaSuccess) return WA_ERR_CUDA;
+    for (const wa::HostBlock& blk : merges)
+      if (copy_block(g, out, dout, blk, cudaMemcpyDeviceToHost, plan->s_out) != cudaSuccess) return WA_ERR_CUDA;
   }
-  // The merge of the global rows' splits needs every launch; then the rows not yet copied back follow.
   if (cudaEventRecord(ev_c2, plan->s_c2) != cudaSuccess || cudaStreamWaitEvent(s, ev_c2, 0) != cudaSuccess)
     return WA_ERR_CUDA;
-  if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
-  if (cudaEventRecord(ev_merged, s) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_merged, 0) != cudaSuccess)
-    return WA_ERR_CUDA;
-  cudaError_t e = cudaSuccess;
-  if (!plan->hs.rows)
-    e = cudaMemcpyAsync(out, dout, span, cudaMemcpyDeviceToHost, plan->s_out);
-  else if (g.G > 0)
-    e = copy_rows(g, out, dout, g.g0, g.g0 + g.G, cudaMemcpyDeviceToHost, plan->s_out);
-  if (e != cudaSuccess) return WA_ERR_CUDA;
+  if (!plan->hs.rows) {
+    // One piece: merge every global row after the launch, then copy the whole of out back.
+    a.head_first = 0;
+    a.head_count = 0;
+    if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
+    if (cudaEventRecord(ev_merged, s) != cudaSuccess || cudaStreamWaitEvent(plan->s_out, ev_merged, 0) != cudaSuccess ||
+        cudaMemcpyAsync(out, dout, span, cudaMemcpyDeviceToHost, plan->s_out) != cudaSuccess)
+      return WA_ERR_CUDA;
+  }
   if (cudaEventRecord(ev_outdone, plan->s_out) != cudaSuccess || cudaStreamWaitEvent(s, ev_outdone, 0) != cudaSuccess ||
       cudaEventRecord(plan->done, s) != cudaSuccess)
     return WA_ERR_CUDA;

@@ -130,12 +130,14 @@ wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const 
  * the plan's layout; page-locked memory lets the copies run asynchronously and overlap the computation). The
  * library keeps device copies of the four tensors in the plan (allocated by the first call: 4 x the layout's span,
  * kept until the plan is freed). When the heads of a sequence row are adjacent in memory (stride_h == D, or H == 1),
- * the sequence is copied in as row pieces, the global rows first and then the frames one chunk at a time (the first
- * piece holds the chunks the first window group reads). After each piece arrives, one launch computes the work items
- * whose rows have all arrived, and the rows of out that launch completes are copied back while later pieces are
- * still arriving. Launches alternate between `stream` and a library-owned compute stream; copies run on two
- * library-owned copy streams; events chain all of them to `stream`. The global rows' merge runs last. Other
- * layouts are copied whole and computed in one launch. Results are identical
+ * the sequence is copied in as row pieces, the global rows first and then the frames one window group at a time
+ * (the first frame piece holds the rows the first window group reads; it and the globals are split into two head
+ * ranges, so that the first launch can start after half of that copy, and the last frame piece into four). After
+ * each piece arrives, one launch computes the work items whose rows have all arrived, and the blocks of out that
+ * launch completes are copied back while later pieces are still arriving; the global rows of a head range are
+ * merged and copied back right after the launch that ran the range's last split items. Launches alternate between `stream` and a library-owned compute stream; copies run on two
+ * library-owned copy streams; events chain all of them to `stream`. Other layouts are copied whole and computed in
+ * one launch, merged, and copied back whole. Results are identical
  * to wa_forward. The call is asynchronous: out is complete when `stream` reaches this point (e.g. after
  * cudaStreamSynchronize); q, k, v and out must stay valid until then.
  * Errors: WA_ERR_INVALID for null pointers or out overlapping an input; WA_ERR_OOM when the device copies cannot
@@ -187,13 +189,14 @@ wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layou
 
 /*
  * Host-only: the piece schedule wa_forward_host uses for this geometry and layout, without touching any device.
- * Pieces are sequence row ranges (all batch entries and heads) in the order they are copied in; after piece p has
- * arrived, launch p runs the work items whose rows have all arrived; after launch p the frame rows of out that it
- * completed are copied back (the global rows, or the whole of out when the pieces are not row blocks, after the
- * merge). Writes min(n_pieces, pieces_cap) pairs {lo, hi} to `pieces`; for each work item, in wa_geometry_describe's
- * order, min(n_items, items_cap) launch indices to `item_launch`; and min(n_out, out_cap) triples {launch, lo, hi}
- * to `out_ranges`. Any of the three may be NULL. *n_pieces and *n_out receive the full counts; *row_pieces is 1
- * when pieces are row blocks (stride_h == D or H == 1), else 0 (one piece: the whole tensors).
+ * Pieces are blocks of sequence rows x heads (all batch entries) in the order they are copied in; after piece p has
+ * arrived, launch p runs the work items whose rows have all arrived; after launch p the blocks of out that it
+ * completed are copied back: frame rows, and the global rows of the heads whose last split item it ran (merged
+ * right behind it). When the pieces are not row blocks, the whole of out is merged and copied back at the end. Writes min(n_pieces, pieces_cap) blocks {lo, hi, h_lo, h_hi} (rows [lo, hi), heads
+ * [h_lo, h_hi)) to `pieces`; for each work item, in wa_geometry_describe's order, min(n_items, items_cap) launch
+ * indices to `item_launch`; and min(n_out, out_cap) blocks {launch, lo, hi, h_lo, h_hi} to `out_ranges`. Any of
+ * the three may be NULL. *n_pieces and *n_out receive the full counts; *row_pieces is 1 when pieces are row blocks
+ * (stride_h == D or H == 1), else 0 (one piece: the whole tensors).
  * Errors: as wa_plan_create for the arguments, WA_ERR_INVALID for a null count pointer.
  */
 wa_status wa_host_schedule_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, int64_t* pieces,

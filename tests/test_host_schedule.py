@@ -1,13 +1,16 @@
 """The host-buffer forward's piece schedule (host only, no GPU).
 
-The sequence is copied in as row pieces and launch p runs after piece p has arrived, so the schedule is correct when
-- the pieces partition the rows [0, L) (every row copied exactly once), the global rows first;
-- every work item runs in the launch of the latest piece holding a row it reads, where the kernel reads whole
-  128-row tiles from the start of each of its ranges (q rows, key segment 0, key segment 1; rows past L read as
-  zeros): earlier would read rows that have not arrived, later would stall the pipeline;
-- every frame row of out is copied back exactly once, after every item that writes it has run (the global rows are
-  copied after the merge);
-and it pipelines: at H3 sizes one piece per window group, the first frame piece no longer than the first group needs.
+The sequence is copied in as pieces (blocks of rows x heads) and launch p runs after piece p has arrived, so the
+schedule is correct when
+- the pieces partition the rows [0, L) x heads [0, H) (every element copied exactly once), the global rows first;
+- every work item runs in the launch of the latest piece holding a row it reads for its head, where the kernel
+  reads whole 128-row tiles from the start of each of its ranges (q rows, key segment 0, key segment 1; rows past L
+  read as zeros): earlier would read rows that have not arrived, later would stall the pipeline;
+- every frame row of out is copied back exactly once per head, after every item that writes it has run (the
+  global rows are copied after the merge);
+and it pipelines: at H3 sizes one piece per window group, with the first group's rows and the globals split into
+two head ranges (the first launch starts after half of that copy) and the last frame piece into four (each
+quarter's global rows are merged and copied back right behind its launch).
 """
 import numpy as np
 import pytest
@@ -40,33 +43,36 @@ def check_schedule(T, S, K, r, G, B, H, D, global_pos, strides=None):
     pieces, launch = sched["pieces"], sched["item_launch"]
     F = T * S
     g0, f0 = (0, G) if global_pos else (F, 0)
-    # pieces partition [0, L)
-    piece_of = np.full(L, -1)
-    for p, (lo, hi) in enumerate(pieces):
-        assert 0 <= lo < hi <= L
-        assert (piece_of[lo:hi] == -1).all(), "pieces overlap"
-        piece_of[lo:hi] = p
-    assert (piece_of >= 0).all(), "a row is never copied"
+    # pieces partition [0, L) x [0, H)
+    piece_of = np.full((L, H), -1, dtype=np.int32)
+    for p, (lo, hi, h_lo, h_hi) in enumerate(pieces):
+        assert 0 <= lo < hi <= L and 0 <= h_lo < h_hi <= H
+        assert (piece_of[lo:hi, h_lo:h_hi] == -1).all(), "pieces overlap"
+        piece_of[lo:hi, h_lo:h_hi] = p
+    assert (piece_of >= 0).all(), "an element is never copied"
     if sched["row_pieces"] and G > 0:
-        assert pieces[0] == (g0, g0 + G)
-    # each item runs exactly when the last piece it reads has arrived
+        assert pieces[0][:2] == (g0, g0 + G) and pieces[0][2] == 0
+    # each item runs exactly when the last piece it reads (for its head) has arrived
     assert len(launch) == len(items)
     for it, p in zip(items, launch):
-        need = max(int(piece_of[lo:hi].max()) for lo, hi in read_ranges(it, L))
+        h = it[0] % H
+        need = max(int(piece_of[lo:hi, h].max()) for lo, hi in read_ranges(it, L))
         assert p == need, (it, p, need)
-    # out rows: each frame row copied back once, after all its writers
+    # out: every row of each head copied back once, after all its writers (a global row: after every split item of
+    # its head, whose partial outputs the merge reads)
     if sched["row_pieces"]:
-        copied = np.full(L, -1)
-        for p, lo, hi in sched["out"]:
-            assert f0 <= lo < hi <= f0 + F
-            assert (copied[lo:hi] == -1).all(), "a row of out is copied back twice"
-            copied[lo:hi] = p
-        assert (copied[f0:f0 + F] >= 0).all(), "a frame row of out is never copied back"
+        copied = np.full((L, H), -1, dtype=np.int32)
+        for p, lo, hi, h_lo, h_hi in sched["out"]:
+            assert 0 <= lo < hi <= L and 0 <= h_lo < h_hi <= H
+            assert (lo, hi) == (g0, g0 + G) or f0 <= lo < hi <= f0 + F
+            assert (copied[lo:hi, h_lo:h_hi] == -1).all(), "a block of out is copied back twice"
+            copied[lo:hi, h_lo:h_hi] = p
+        assert (copied >= 0).all(), "a row of out is never copied back"
         for it, p in zip(items, launch):
-            if it[1] == 0:  # window item: writes out rows [q_lo, q_hi)
-                assert (copied[it[2]:it[3]] >= p).all(), "out rows copied back before their item ran"
+            rows = slice(it[2], it[3]) if it[1] == 0 else slice(g0, g0 + G)
+            assert (copied[rows, it[0] % H] >= p).all(), "out rows copied back before an item they need ran"
     else:
-        assert pieces == [(0, L)] and sched["out"] == [] and set(launch) <= {0}
+        assert pieces == [(0, L, 0, H)] and sched["out"] == [] and set(launch) <= {0}
     return L, info, groups, sched
 
 
@@ -109,15 +115,28 @@ def test_schedule_pipelines_h3():
     KS = w.K * w.S
     pieces = sched["pieces"]
     assert sched["row_pieces"]
-    # the globals, then one piece per window group, ending where its reads end; the last two groups (windows
-    # [31, 33] and [32, 33]) both read to the end of the frames and share the last piece
-    assert info["n_groups"] == 34 and len(pieces) == 1 + 33
-    # the first frame piece: the chunks the first group reads (chunks 0..r) and at most one tile more
-    assert pieces[1][0] == 0 and (w.r + 1) * KS <= pieces[1][1] <= (w.r + 1) * KS + TILE
-    # later frame pieces hold about one chunk each
-    assert all(abs((hi - lo) - KS) <= TILE for lo, hi in pieces[2:-1])
+    half = w.H // 2
+    # the globals and the first window group's rows, each in two head ranges, alternating so that the first
+    # group's first heads can start after half of that copy
+    assert [p[2:] for p in pieces[:4]] == [(0, half), (0, half), (half, w.H), (half, w.H)]
+    assert pieces[0][:2] == pieces[2][:2] == (w.L - w.G, w.L)
+    first = pieces[1][:2]
+    assert pieces[3][:2] == first and first[0] == 0 and (w.r + 1) * KS <= first[1] <= (w.r + 1) * KS + TILE
+    # then one piece per window group (all heads), ending where its reads end; the last two groups (windows
+    # [31, 33] and [32, 33]) both read to the end of the frames and share the last piece, which comes in four head
+    # ranges
+    quarter = [(w.H * i // 4, w.H * (i + 1) // 4) for i in range(4)]
+    assert info["n_groups"] == 34 and len(pieces) == 4 + 31 + 4
+    assert all(p[2:] == (0, w.H) for p in pieces[4:-4])
+    assert [p[2:] for p in pieces[-4:]] == quarter and len({p[:2] for p in pieces[-4:]}) == 1
+    assert pieces[-1][1] == w.L - w.G
+    assert all(abs((hi - lo) - KS) <= TILE for lo, hi, _, _ in pieces[4:-4])
+    # the global rows of each quarter of the heads are merged and copied back right behind that quarter's launch
+    merges = [o for o in sched["out"] if o[1:3] == (w.L - w.G, w.L)]
+    assert [o[3:] for o in merges] == quarter and [o[0] for o in merges] == list(range(len(pieces) - 4, len(pieces)))
     launches = sched["item_launch"]
-    assert max(launches) == len(pieces) - 1 and min(launches) >= 1  # piece 0 (globals) alone runs nothing
+    assert max(launches) == len(pieces) - 1
+    assert min(launches) == 1  # the first window group's first heads run after the second piece
 
 
 def test_schedule_caps_the_piece_count():
