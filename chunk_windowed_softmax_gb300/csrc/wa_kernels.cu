@@ -66,19 +66,26 @@ struct Cfg {
   static constexpr int kSKSteps = kF8 ? D / 32 : D / 16;       // score MMAs per tile (32 bytes of K each)
   static_assert(kQKBoxes >= 1 && kQKRowBytes % 128 == 0, "q / k rows must be whole 128-byte boxes");
   // Separate K and V rings; the producer runs K one tile ahead of V (K is needed a step earlier than V).
-  static constexpr int kKSlots = kF8 ? 5 : (D == 128 ? 3 : 4);
+  static constexpr int kKSlots = kF8 ? 5 : (D == 128 ? 2 : 4);
   static constexpr int kVSlots = kF8 ? 3 : (D == 128 ? 2 : 4);
   // Step bundles: the copies of step j (K_j and V_{j-1}) complete on one barrier and are released by one commit.
   // Bundle b reuses a K slot last read in bundle <= b - kKSlots and a V slot last read in bundle <= b - kVSlots,
   // so the producer waits for bundle b - kLag's release, kLag = min(kKSlots, kVSlots) (also the barrier count).
   static constexpr int kLag = kKSlots < kVSlots ? kKSlots : kVSlots;
+  // bf16 D = 128: full window tiles leave through shared memory and one TMA store per 64 columns (16 KB per query
+  // tile: each store instruction of the softmax warps then fills whole 128-byte rows of shared memory, instead of
+  // touching 32 rows of out); with bundled barriers a third K slot would never be reused sooner than the second, so
+  // its 32 KB hold the two tiles' staging.
+  static constexpr bool kStage = D == 128 && !kF8;
+  static constexpr int kStageTileBytes = kTileRows * 128;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kQTileBytes;
   static constexpr int kVOff = kKOff + kKSlots * kQTileBytes;
-  static constexpr int kBarOff = kVOff + kVSlots * kVTileBytes;
+  static constexpr int kStageOff = kVOff + kVSlots * kVTileBytes;
+  static constexpr int kBarOff = kStageOff + (kStage ? 2 * kStageTileBytes : 0);
   // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain b_full[kLag] b_empty[kLag]
-  //           item ring full[kItemRingSlots] empty[kItemRingSlots]
-  static constexpr int kNumBars = 11 + 2 * kLag + 2 * kItemRingSlots;
+  //           item ring full[kItemRingSlots] empty[kItemRingSlots]  stage_full[2] stage_free[2]
+  static constexpr int kNumBars = 11 + 2 * kLag + 2 * kItemRingSlots + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
   static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kItemRingSlots + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t kTmemO = 256;
@@ -121,6 +128,11 @@ struct BarAddr {
   __device__ __forceinline__ uint32_t b_empty(uint32_t b) const { return base + 8 * (11 + NB + b % NB); }
   // the work-item ring's barriers (ItemFeed)
   __device__ __forceinline__ uint32_t item_ring() const { return base + 8 * (11 + 2 * NB); }
+  // query tile t's epilogue staging: written by its 4 warps (full), read out by the store (free)
+  __device__ __forceinline__ uint32_t stage_full(int t) const { return base + 8 * (11 + 2 * NB + 2 * kItemRingSlots + t); }
+  __device__ __forceinline__ uint32_t stage_free(int t) const {
+    return base + 8 * (13 + 2 * NB + 2 * kItemRingSlots + t);
+  }
 };
 
 // Exponentiate one 128-column score row into bf16 P (written to TMEM over the row's S columns, 16 columns per
@@ -147,7 +159,8 @@ __device__ __forceinline__ float exp_store_row(const float (&s)[128], float c_sc
 template <int D, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     window_attention_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                            const __grid_constant__ CUtensorMap tmap_v, const Params prm) {
+                            const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                            const Params prm) {
   using C = Cfg<D, kF8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.b_empty(s), 1);
     }
     feed.init(kItemConsumers);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.stage_full(t), 4);  // one arrive per warp of the tile's warpgroup
+      mbar_init(bars.stage_free(t), 1);  // the store issuer, once the copy engine has read the stage
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -380,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + C::kTmemO + t * 128;
     const uint32_t bar_s = bars.s_full(t), bar_p = bars.p_full(t), bar_o = bars.o_full(t);
-    uint32_t s_n = 0, o_n = 0;
+    uint32_t s_n = 0, o_n = 0, st_n = 0;  // st_n: staged halves of this warpgroup
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
       const int idx = feed.fetch(n, abort_flag, err, ok);  // every softmax warp takes every item
@@ -461,7 +478,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = row < it.q_hi;
       const float inv_l = 1.f / l;
       const int b = it.bh / prm.H, h = it.bh % prm.H;
-      if (it.split < 0) {
+      const int row0 = it.q_lo + t * kTileRows;
+      if (C::kStage && it.split < 0 && row0 + kTileRows <= it.q_hi) {
+        // A full tile: each 64-column half is written to this tile's stage in the store's 128-byte swizzle, then
+        // one thread of the warpgroup stores it with TMA once all four warps have written their rows.
+        const uint32_t stage = s_base + C::kStageOff + t * C::kStageTileBytes;
+        const bool issuer = (warp & 3) == 0 && lane == 0;
+#pragma unroll 1
+        for (int half = 0; half < 2 && ok; ++half) {
+          ok = mbar_wait(bars.stage_free(t), (st_n & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          const uint32_t row_addr = stage + row_in_tile * 128;
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + half * 64 + c0, o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // 16-byte chunk c of the row sits at chunk c ^ (row % 8)
+              const int c = c0 / 8 + q;
+              sts_u4(row_addr + ((c ^ (row_in_tile & 7)) << 4),
+                     pack_bf16(__uint_as_float(o[8 * q]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l),
+                     pack_bf16(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l),
+                     pack_bf16(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l),
+                     pack_bf16(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l));
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.stage_full(t));
+          if (issuer) {
+            ok = mbar_wait(bars.stage_full(t), st_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            if (ok) {
+              tma_store_4d(&tmap_o, stage, half * 64, h, row0, b);
+              bulk_commit();
+              bulk_wait_read();
+              mbar_arrive(bars.stage_free(t));
+            }
+          }
+          ok = __all_sync(0xffffffffu, ok);
+          st_n++;
+        }
+        if (prm.lse != nullptr)  // m and l are in log2 units of the scaled score
+          prm.lse[(int64_t)it.bh * prm.L + row] = (m + __log2f(l)) * 0.6931471805599453f;
+      } else if (it.split < 0) {
         __nv_bfloat16* dst = prm.out + (int64_t)b * prm.sb + (int64_t)row * prm.sl + (int64_t)h * prm.sh;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -499,6 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     }
+    // The warpgroup's last stores must have written out (and read their stage) before the CTA leaves.
+    if (C::kStage && (warp & 3) == 0 && lane == 0) bulk_wait();
     teardown();
   }
 }
@@ -579,10 +641,10 @@ int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const int qk_bytes = kF8 ? 1 : 2;
   if (!make_map(&mq, a.q, *a.geo, qk_bytes) || !make_map(&mk, a.k, *a.geo, qk_bytes) ||
-      !make_map(&mv, a.v, *a.geo, 2))
+      !make_map(&mv, a.v, *a.geo, 2) || !make_map(&mo, a.out, *a.geo, 2))
     return (int)cudaErrorInvalidValue;
   const wa_layout_t& l = a.geo->layout;
   Params p;
@@ -605,7 +667,7 @@ int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
   p.L = (int)a.geo->L;
   p.item_counter = a.item_counter;
   const int grid = a.n_items < num_sms ? a.n_items : num_sms;
-  window_attention_kernel<D, kF8><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
+  window_attention_kernel<D, kF8><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mo, p);
   return (int)cudaGetLastError();
 }
 
