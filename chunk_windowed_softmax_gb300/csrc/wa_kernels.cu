@@ -66,17 +66,17 @@ struct Cfg {
   static constexpr int kSKSteps = kF8 ? D / 32 : D / 16;       // score MMAs per tile (32 bytes of K each)
   static_assert(kQKBoxes >= 1 && kQKRowBytes % 128 == 0, "q / k rows must be whole 128-byte boxes");
   // Separate K and V rings; the producer runs K one tile ahead of V (K is needed a step earlier than V).
-  static constexpr int kKSlots = kF8 ? 5 : (D == 128 ? 2 : 4);
+  static constexpr int kKSlots = kF8 ? 3 : (D == 128 ? 2 : 4);
   static constexpr int kVSlots = kF8 ? 3 : (D == 128 ? 2 : 4);
   // Step bundles: the copies of step j (K_j and V_{j-1}) complete on one barrier and are released by one commit.
   // Bundle b reuses a K slot last read in bundle <= b - kKSlots and a V slot last read in bundle <= b - kVSlots,
   // so the producer waits for bundle b - kLag's release, kLag = min(kKSlots, kVSlots) (also the barrier count).
   static constexpr int kLag = kKSlots < kVSlots ? kKSlots : kVSlots;
-  // bf16 D = 128: full window tiles leave through shared memory and one TMA store per 64 columns (16 KB per query
-  // tile: each store instruction of the softmax warps then fills whole 128-byte rows of shared memory, instead of
-  // touching 32 rows of out); with bundled barriers a third K slot would never be reused sooner than the second, so
-  // its 32 KB hold the two tiles' staging.
-  static constexpr bool kStage = D == 128 && !kF8;
+  // D = 128: full window tiles leave through shared memory and one TMA store per 64 columns (16 KB per query tile:
+  // each store instruction of the softmax warps then fills whole 128-byte rows of shared memory, instead of
+  // touching 32 rows of out). A bundle's K slot is never reused sooner than kLag bundles later, so K slots beyond
+  // kLag would sit idle: their space holds the two tiles' staging.
+  static constexpr bool kStage = D == 128;
   static constexpr int kStageTileBytes = kTileRows * 128;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kQTileBytes;
