@@ -15,6 +15,7 @@
 //               V_{j-1} complete on one bundle barrier. It also claims the CTA's next work item from a global
 //               counter when it is ready for one, and passes the index to the other roles through a shared ring
 //   warps 10-11 idle
+// Full window tiles (D = 128) leave through a shared-memory stage and TMA stores; the rest is stored directly.
 // The launch gives every thread 168 registers (384 x 168 = 64512); setmaxnreg then moves them to where the work
 // is: the softmax warpgroups rise to 192 (a full 128-column score row stays in registers), the third warpgroup
 // drops to 120. 2 x 128 x 192 + 128 x 120 = 64512, the launch's total. Each role branch ends with its own copy of
