@@ -90,6 +90,8 @@ GRAD_CASES = [
     configs.Workload("bwd_radius_covers_all", B=1, H=2, D=128, T=7, S=90, K=2, r=9, G=40, global_pos=0, seed=47),
     configs.Workload("bwd_sharp_globals", B=1, H=2, D=128, T=12, S=64, K=3, r=1, G=256, global_pos=0, seed=48,
                      k_global_scale=4.0),
+    # at least 1024 global rows: doubled split length (2 splits), partial last global tile
+    configs.Workload("bwd_long_globals", B=1, H=2, D=128, T=40, S=64, K=1, r=0, G=1100, global_pos=0, seed=49),
 ]
 
 

@@ -101,6 +101,8 @@ PIECE_CASES = [
     (configs.Workload("host_lbhd", B=2, H=2, D=64, T=10, S=30, K=3, r=1, G=16, global_pos=1, seed=68), "lbhd"),
     (configs.Workload("host_one_head_rowpad", B=1, H=1, D=128, T=12, S=33, K=1, r=3, G=7, global_pos=0, seed=69),
      "rowpad"),
+    (configs.Workload("host_long_globals", B=1, H=8, D=128, T=40, S=64, K=1, r=0, G=1100, global_pos=0, seed=70),
+     None),  # 2 global splits; the head ranges of the first and last pieces merge their global rows separately
 ]
 
 

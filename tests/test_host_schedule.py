@@ -87,6 +87,7 @@ GEOMETRIES = [
     (300, 1, 7, 2, 5, 1, 3, 128, 1),      # one-token frames
     (11, 40, 2, 2, 24, 2, 3, 128, 0),
     (5, 200, 1, 0, 300, 1, 1, 64, 0),     # r = 0: each group's last query tile reads past its own chunk
+    (40, 64, 1, 0, 1100, 1, 8, 128, 0),   # 1100 global rows: doubled split length, per-head-range merges
 ]
 
 

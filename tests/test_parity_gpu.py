@@ -89,6 +89,10 @@ EDGE = [
     # frames' reference max overflow, and the softmax must raise its reference in the middle of an item
     configs.Workload("score_jump", B=1, H=2, D=64, T=10, S=64, K=2, r=2, G=128, global_pos=0, seed=22,
                      k_global_scale=16.0),
+    # at least 1024 global rows: the global leg's splits are twice the longest window item (2 splits here, not 3 or
+    # 4), and the last global query tile is partial
+    configs.Workload("long_globals", B=1, H=2, D=128, T=40, S=64, K=1, r=0, G=1100, global_pos=0, seed=23),
+    configs.Workload("long_globals_front_d64", B=2, H=1, D=64, T=60, S=50, K=1, r=0, G=1030, global_pos=1, seed=24),
 ]
 
 
