@@ -478,11 +478,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //                          Phase A: P^T = 2^(s c' - lse'_col) -> bf16 into TMEM. Phase B: dS^T = P^T (dP^T - Dvec_col)
 //                          -> bf16 into TMEM. P stays in fp32 registers between the phases.
 //   warp 4 kCG            MMA issuer: S^T = K Q^T, dP^T = V dout^T, dv += P^T dout, dk += dS^T Q
-//   warp 4 kCG + 1        idle (the dq kernel's second issuer; both kernels share one launch shape)
+//   warp 4 kCG + 1        query-tile loader (the dq kernel's second issuer; both kernels share one launch shape):
+//                          lane 0 issues the TMA copies of the query tiles into their own ring
 //   warp 4 kCG + 2        loads (all lanes): lane 0 issues the TMA copies (the key / value tiles of the sub-item and
-//                          a ring of query / dout tiles); every lane then stages 4 query columns' values
-//                          (log2-domain lse, Dvec) into the ring slot. Columns past the segment get lse' = +inf and
-//                          Dvec = 0, so their P and dS are exactly 0 with no masking in the elementwise code.
+//                          a ring of dout tiles); every lane then stages 4 query columns' values (log2-domain lse,
+//                          Dvec, both negated) into the dout slot. Columns past the segment get -lse' = -inf and
+//                          -Dvec = 0, so their P and dS are exactly 0 with no masking in the elementwise code.
 // TMEM: S^T [0,128) (P^T packed over the front of each group's columns), dP^T [128,256) (dS^T likewise),
 // dv [256, 256+D), dk [384, 384+D). Issue order per step n: dv(n) after P^T(n) is written, then S^T(n+1); dk(n)
 // after dS^T(n), then dP^T(n+1). So the tensor core computes dv(n) and S^T(n+1) while the elementwise warps work on
@@ -491,17 +492,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D>
 struct DkvCfg {
   static constexpr int kTileBytes = kTileRows * D * 2;
-  static constexpr int kQSlots = D == 128 ? 2 : 3;  // ring of (query tile, dout tile, column values)
-  static constexpr int kSlotBytes = 2 * kTileBytes;
+  // Two rings, each filled by its own loader warp: query tiles (read by S^T(j) and dk(j)) and dout tiles with the
+  // per-column values (read by dP^T(j), dv(j) and the elementwise phases). A query tile's slot is free once dk of
+  // the tile kQSlots steps back has completed, early enough for the copy to land before S^T needs it.
+  static constexpr int kQSlots = D == 128 ? 3 : 4;
+  static constexpr int kDSlots = D == 128 ? 2 : 3;
   static constexpr int kKOff = 0, kVOff = kTileBytes;
-  static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kColOff = kRingOff + kQSlots * kSlotBytes;  // per slot: lse'[128] then Dvec[128], fp32
+  static constexpr int kQOff = 2 * kTileBytes;
+  static constexpr int kDOOff = kQOff + kQSlots * kTileBytes;
+  // per dout slot: -lse'[128] then -Dvec[128], fp32 (negated so that the elementwise warps add them with packed
+  // f32x2 instructions)
+  static constexpr int kColOff = kDOOff + kDSlots * kTileBytes;
   static constexpr int kColBytes = 64 * 16;
-  static constexpr int kBarOff = kColOff + kQSlots * kColBytes;
-  // kv_full, kv_empty, s_full, p_full, dp_full, ds_full, o_full, drain_x, then q_full[slots], q_empty[slots]
-  static constexpr int kNumBars = 8 + 2 * kQSlots + 2 * kItemRingSlots;  // the last 2 kItemRingSlots: ItemFeed
+  static constexpr int kBarOff = kColOff + kDSlots * kColBytes;
+  // kv_full, kv_empty, s_full, p_full, dp_full, ds_full, o_full, drain_x, q_full[], q_empty[], d_full[], d_empty[],
+  // then the ItemFeed's 2 kItemRingSlots
+  static constexpr int kNumBars = 8 + 2 * kQSlots + 2 * kDSlots + 2 * kItemRingSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
-  static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kItemRingSlots + 1024;
+  static constexpr int kUsed = kMiscOff + 16 + 4 * kItemRingSlots;
+  // Room to realign the window to 1024 bytes where it fits; otherwise the window itself must be aligned (checked
+  // at launch).
+  static constexpr int kSlack = kUsed + 1024 <= 232448 ? 1024 : 0;
+  static constexpr int kSmemBytes = kUsed + kSlack;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
   static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 0, 1);  // A from TMEM, query-side tile MN-major
@@ -514,14 +526,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    const BwdParams prm) {
   using C = DkvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (C::kSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {  // no room to realign: report, touch nothing
+    if (threadIdx.x == 0) atomicOr(prm.err, kErrBounds);
+    return;
+  }
   const Smem sm = align_smem(smem_raw);
-  const uint32_t sK = sm.base + C::kKOff, sV = sm.base + C::kVOff, sRing = sm.base + C::kRingOff;
+  const uint32_t sK = sm.base + C::kKOff, sV = sm.base + C::kVOff, sQ = sm.base + C::kQOff, sDO = sm.base + C::kDOOff;
   const uint32_t sCol = sm.base + C::kColOff;
   const uint32_t bar = sm.base + C::kBarOff;
   const uint32_t b_kvfull = bar, b_kvempty = bar + 8, b_sfull = bar + 16, b_pfull = bar + 24, b_dpfull = bar + 32,
                  b_dsfull = bar + 40, b_ofull = bar + 48, b_drain_x = bar + 56;
   auto b_qfull = [&](uint32_t s) { return bar + 8 * (8 + s); };
   auto b_qempty = [&](uint32_t s) { return bar + 8 * (8 + C::kQSlots + s); };
+  auto b_dfull = [&](uint32_t s) { return bar + 8 * (8 + 2 * C::kQSlots + s); };
+  auto b_dempty = [&](uint32_t s) { return bar + 8 * (8 + 2 * C::kQSlots + C::kDSlots + s); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
   const ItemFeed feed{prm.item_counter, prm.n_items, reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 16),
@@ -539,10 +557,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(b_ofull, 1);
     mbar_init(b_drain_x, 1);
     for (int s = 0; s < C::kQSlots; ++s) {
-      mbar_init(b_qfull(s), 1 + 32);  // the copies' expect-tx arrival + one per loader lane (column values)
-      mbar_init(b_qempty(s), 1 + kEwWarps);  // the MMA commit after dk(j) + one per elementwise warp
+      mbar_init(b_qfull(s), 1);   // the copy's expect-tx arrival
+      mbar_init(b_qempty(s), 1);  // the MMA commit after dk(j)
     }
-    feed.init(kEwWarps + 1);  // item consumers: the issuer, the elementwise warps
+    for (int s = 0; s < C::kDSlots; ++s) {
+      mbar_init(b_dfull(s), 1 + 32);         // the copy's expect-tx arrival + one per loader lane (column values)
+      mbar_init(b_dempty(s), 1 + kEwWarps);  // the MMA commit after dv(j) + one per elementwise warp
+    }
+    feed.init(kEwWarps + 2);  // item consumers: the issuer, the query-tile loader, the elementwise warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -557,8 +579,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
 
   if (warp == kLoadWarp) {
-    // ------------------------------------------------------------------------------------------- loaders
-    uint32_t kv_n = 0, q_n = 0;
+    // ---------------------------------------------------------------- key/value, dout and column-value loader
+    uint32_t kv_n = 0, d_n = 0;
     bool ok = true, dropped = false;
     for (uint32_t n = 0; ok; ++n) {
       const int idx = feed.claim_warp(n, abort_flag, err, ok);
@@ -588,34 +610,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int c = 4 * lane + i;
-            l4[i] = c < valid ? __ldg(lse_bh + row + c) * kLog2e : INFINITY;
-            d4[i] = c < valid ? __ldg(dv_bh + row + c) : 0.f;
+            l4[i] = c < valid ? -__ldg(lse_bh + row + c) * kLog2e : -INFINITY;
+            d4[i] = c < valid ? -__ldg(dv_bh + row + c) : 0.f;
           }
-          const uint32_t qs = q_n % C::kQSlots;
-          ok = mbar_wait(b_qempty(qs), ((q_n / C::kQSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          const uint32_t ds = d_n % C::kDSlots;
+          ok = mbar_wait(b_dempty(ds), ((d_n / C::kDSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           if (lane == 0) {
-            if ((prm.debug_flags & 4) && !dropped && blockIdx.x == 0) {
+            mbar_arrive_expect_tx(b_dfull(ds), C::kTileBytes);
+            if ((prm.debug_flags & 4) && !dropped && blockIdx.x == 0)
               dropped = true;  // fault injection for the watchdog test: bytes expected, no copy issued
-              mbar_arrive_expect_tx(b_qfull(qs), C::kSlotBytes);
-            } else {
-              const uint32_t dst = sRing + qs * C::kSlotBytes;
-              mbar_arrive_expect_tx(b_qfull(qs), C::kSlotBytes);
-              load_tile<D>(dst, &tm_q, b_qfull(qs), h, row, b);
-              load_tile<D>(dst + C::kTileBytes, &tm_do, b_qfull(qs), h, row, b);
-            }
+            else
+              load_tile<D>(sDO + ds * C::kTileBytes, &tm_do, b_dfull(ds), h, row, b);
           }
-          const uint32_t cb = sCol + qs * C::kColBytes + 16 * lane;
+          const uint32_t cb = sCol + ds * C::kColBytes + 16 * lane;
           sts_f4(cb, make_float4(l4[0], l4[1], l4[2], l4[3]));
           sts_f4(cb + 512, make_float4(d4[0], d4[1], d4[2], d4[3]));
-          mbar_arrive(b_qfull(qs));  // release: the column values are visible to whoever waits on q_full
-          q_n++;
+          mbar_arrive(b_dfull(ds));  // release: the column values are visible to whoever waits on d_full
+          d_n++;
         }
       }
     }
     if (!ok && lane == 0) {
       if (kv_n) mbar_wait_drain(b_kvfull, (kv_n - 1) & 1, kDrainLimitNs);
+      for (uint32_t n = d_n > (uint32_t)C::kDSlots ? d_n - C::kDSlots : 0; n < d_n; ++n)
+        mbar_wait_drain(b_dfull(n % C::kDSlots), (n / C::kDSlots) & 1, kDrainLimitNs);
+    }
+  } else if (warp == kMmaWarpY) {
+    // ------------------------------------------------------------------------------------- query-tile loader
+    uint32_t q_n = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      const int idx = feed.fetch(n, abort_flag, err, ok);
+      if (idx < 0) break;
+      const Item it = load_item(prm.items, idx);
+      const int b = it.bh / prm.H, h = it.bh % prm.H;
+      const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
+      const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
+      const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
+      for (int t = 0; t < ntk && ok; ++t) {
+        for (int j = 0; j < nt && ok; ++j) {
+          int valid;
+          const int row = step_row(it, j, nt0, &valid);
+          const uint32_t qs = q_n % C::kQSlots;
+          ok = mbar_wait(b_qempty(qs), ((q_n / C::kQSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(b_qfull(qs), C::kTileBytes);
+            load_tile<D>(sQ + qs * C::kTileBytes, &tm_q, b_qfull(qs), h, row, b);
+          }
+          q_n++;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
       for (uint32_t n = q_n > (uint32_t)C::kQSlots ? q_n - C::kQSlots : 0; n < q_n; ++n)
         mbar_wait_drain(b_qfull(n % C::kQSlots), (n / C::kQSlots) & 1, kDrainLimitNs);
     }
@@ -626,11 +676,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // chain dv(j) -> S^T(j+1) -> phase A stays on one thread either way, and the other thread's products then
     // compete with it on the tensor core.)
     {  // the whole warp runs the issue loop; one elected lane issues (issue model in wa_ptx.cuh)
-      uint32_t kv_n = 0, q_n = 0, p_n = 0, ds_n = 0;
+      uint32_t kv_n = 0, q_n = 0, d_n = 0, p_n = 0, ds_n = 0;
       bool ok = true;
       const uint64_t dk_ = sdesc_sw128(sK, 16, 1024), dv_ = sdesc_sw128(sV, 16, 1024);
-      const uint64_t dr_k = sdesc_sw128(sRing, 16, 1024);                // ring tiles as K-major B (S^T, dP^T)
-      const uint64_t dr_mn = sdesc_sw128(sRing, kTileRows * 128, 1024);  // ring tiles as MN-major B (dv, dk)
+      const uint64_t dq_k = sdesc_sw128(sQ, 16, 1024), dd_k = sdesc_sw128(sDO, 16, 1024);  // K-major B (S^T, dP^T)
+      const uint64_t dq_mn = sdesc_sw128(sQ, kTileRows * 128, 1024);  // MN-major B (dk)
+      const uint64_t dd_mn = sdesc_sw128(sDO, kTileRows * 128, 1024);  // MN-major B (dv)
       const uint32_t hi = (uint32_t)(dk_ >> 32);
       auto issue_nt = [&](uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
 #pragma unroll
@@ -646,8 +697,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ts(d_tmem, a_tmem + tmem_a_block(kk), b_lo + ((kk * 2048) >> 4), hi, C::kIdescAcc,
                  (acc || kk > 0) ? 1u : 0u);
       };
-      auto slot_k = [&](uint32_t s, uint32_t tile) { return (uint32_t)dr_k + ((s * C::kSlotBytes + tile) >> 4); };
-      auto slot_mn = [&](uint32_t s, uint32_t tile) { return (uint32_t)dr_mn + ((s * C::kSlotBytes + tile) >> 4); };
+      auto tile_at = [&](uint64_t desc, uint32_t s) { return (uint32_t)desc + ((s * C::kTileBytes) >> 4); };
       for (uint32_t n = 0; ok; ++n) {
         const int idx = feed.fetch(n, abort_flag, err, ok);
         if (idx < 0) break;
@@ -657,14 +707,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int t = 0; t < ntk && ok; ++t) {
           ok = mbar_wait_warp(b_kvfull, kv_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           kv_n++;
-          uint32_t qs = q_n % C::kQSlots;
+          uint32_t qs = q_n % C::kQSlots, ds = d_n % C::kDSlots;
           ok = ok && mbar_wait_warp(b_qfull(qs), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           q_n++;
           if (!ok) break;
           tc_fence_after();
-          issue_nt(tS, (uint32_t)dk_, slot_k(qs, 0));  // S^T(0) = K Q_0^T
+          issue_nt(tS, (uint32_t)dk_, tile_at(dq_k, qs));  // S^T(0) = K Q_0^T
           mma_commit(b_sfull);
-          issue_nt(tDP, (uint32_t)dv_, slot_k(qs, C::kTileBytes));  // dP^T(0) = V dout_0^T
+          ok = mbar_wait_warp(b_dfull(ds), (d_n / C::kDSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          d_n++;
+          if (!ok) break;
+          tc_fence_after();
+          issue_nt(tDP, (uint32_t)dv_, tile_at(dd_k, ds));  // dP^T(0) = V dout_0^T
           mma_commit(b_dpfull);
           if (nt == 1) mma_commit(b_kvempty);
           for (int j = 0; j < nt && ok; ++j) {
@@ -672,29 +726,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             p_n++;
             if (!ok) break;
             tc_fence_after();
-            issue_acc(tDV, tS, slot_mn(qs, C::kTileBytes), j > 0);  // dv += P^T(j) dout_j
-            uint32_t qn = 0;
+            issue_acc(tDV, tS, tile_at(dd_mn, ds), j > 0);  // dv += P^T(j) dout_j
+            mma_commit(b_dempty(ds));  // dout_j is read for the last time (its column values: elementwise warps)
+            uint32_t qn = 0, dn = 0;
             if (j + 1 < nt) {
               qn = q_n % C::kQSlots;
               ok = mbar_wait_warp(b_qfull(qn), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
               q_n++;
               if (!ok) break;
               tc_fence_after();
-              issue_nt(tS, (uint32_t)dk_, slot_k(qn, 0));  // S^T(j+1)
+              issue_nt(tS, (uint32_t)dk_, tile_at(dq_k, qn));  // S^T(j+1)
               mma_commit(b_sfull);
             }
             ok = mbar_wait_warp(b_dsfull, ds_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);  // dS^T(j) in TMEM
             ds_n++;
             if (!ok) break;
             tc_fence_after();
-            issue_acc(tDK, tDP, slot_mn(qs, 0), j > 0);  // dk += dS^T(j) Q_j
+            issue_acc(tDK, tDP, tile_at(dq_mn, qs), j > 0);  // dk += dS^T(j) Q_j
             mma_commit(b_qempty(qs));
             if (j + 1 < nt) {
-              issue_nt(tDP, (uint32_t)dv_, slot_k(qn, C::kTileBytes));  // dP^T(j+1)
+              dn = d_n % C::kDSlots;
+              ok = mbar_wait_warp(b_dfull(dn), (d_n / C::kDSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              d_n++;
+              if (!ok) break;
+              tc_fence_after();
+              issue_nt(tDP, (uint32_t)dv_, tile_at(dd_k, dn));  // dP^T(j+1)
               mma_commit(b_dpfull);
               if (j + 1 == nt - 1) mma_commit(b_kvempty);  // every MMA that reads the key / value tiles is issued
             }
             qs = qn;
+            ds = dn;
           }
           if (!ok) break;
           mma_commit(b_ofull);
@@ -708,7 +769,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = 32 * (warp & 3) + lane;  // key row in the tile == TMEM lane
     const int col0 = kCW * (warp >> 2);   // this thread's query columns [col0, col0 + kCW)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    uint32_t q_n = 0, s_n = 0, o_n = 0;
+    uint32_t d_n = 0, s_n = 0, o_n = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
       const int idx = feed.fetch(n, abort_flag, err, ok);
@@ -718,14 +779,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int nt = seg_tiles(it.s0_lo, it.s0_hi) + seg_tiles(it.s1_lo, it.s1_hi);
       for (int t = 0; t < ntk && ok; ++t) {
         for (int j = 0; j < nt; ++j) {
-          const uint32_t qs = q_n % C::kQSlots;
-          ok = mbar_wait(b_qfull(qs), (q_n / C::kQSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          const uint32_t ds = d_n % C::kDSlots;
+          ok = mbar_wait(b_dfull(ds), (d_n / C::kDSlots) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           ok = ok && mbar_wait(b_sfull, s_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           ok = __all_sync(0xffffffffu, ok);
-          q_n++;
+          d_n++;
           if (!ok) break;
           tc_fence_after();
-          const uint32_t cb = sCol + qs * C::kColBytes + col0 * 4;  // lse' of this thread's first column
+          const uint32_t cb = sCol + ds * C::kColBytes + col0 * 4;  // -lse' of this thread's first column
           // Phase A: P^T = 2^(s c' - lse'_col) over this thread's query columns
           float p[kCW];
 #pragma unroll
@@ -734,12 +795,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_ld_x32(tS + lane_base + col0 + 32 * ch, sr);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 lv = lds_f4(cb + (32 * ch + 4 * c4) * 4);  // lse' of 4 columns
+              const float4 nl = lds_f4(cb + (32 * ch + 4 * c4) * 4);  // -lse' of 4 columns
               const int i = 32 * ch + 4 * c4;
-              p[i] = ex2(fmaf(__uint_as_float(sr[4 * c4]), prm.c_log2, -lv.x));
-              p[i + 1] = ex2(fmaf(__uint_as_float(sr[4 * c4 + 1]), prm.c_log2, -lv.y));
-              p[i + 2] = ex2(fmaf(__uint_as_float(sr[4 * c4 + 2]), prm.c_log2, -lv.z));
-              p[i + 3] = ex2(fmaf(__uint_as_float(sr[4 * c4 + 3]), prm.c_log2, -lv.w));
+              float x0, x1, x2, x3;
+              fma2(x0, x1, __uint_as_float(sr[4 * c4]), __uint_as_float(sr[4 * c4 + 1]), prm.c_log2, prm.c_log2, nl.x,
+                   nl.y);
+              fma2(x2, x3, __uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3]), prm.c_log2, prm.c_log2,
+                   nl.z, nl.w);
+              p[i] = ex2(x0);
+              p[i + 1] = ex2(x1);
+              p[i + 2] = ex2(x2);
+              p[i + 3] = ex2(x3);
               pk[2 * c4] = pack_bf16(p[i], p[i + 1]);
               pk[2 * c4 + 1] = pack_bf16(p[i + 2], p[i + 3]);
             }
@@ -761,12 +827,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_ld_x32(tDP + lane_base + col0 + 32 * ch, dr);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 dv4 = lds_f4(cb + 512 + (32 * ch + 4 * c4) * 4);  // Dvec of 4 columns
+              const float4 nd = lds_f4(cb + 512 + (32 * ch + 4 * c4) * 4);  // -Dvec of 4 columns
               const int i = 32 * ch + 4 * c4;
-              pk[2 * c4] = pack_bf16(p[i] * (__uint_as_float(dr[4 * c4]) - dv4.x),
-                                     p[i + 1] * (__uint_as_float(dr[4 * c4 + 1]) - dv4.y));
-              pk[2 * c4 + 1] = pack_bf16(p[i + 2] * (__uint_as_float(dr[4 * c4 + 2]) - dv4.z),
-                                         p[i + 3] * (__uint_as_float(dr[4 * c4 + 3]) - dv4.w));
+              float t0, t1, t2, t3;
+              add2(t0, t1, __uint_as_float(dr[4 * c4]), __uint_as_float(dr[4 * c4 + 1]), nd.x, nd.y);
+              add2(t2, t3, __uint_as_float(dr[4 * c4 + 2]), __uint_as_float(dr[4 * c4 + 3]), nd.z, nd.w);
+              mul2(t0, t1, t0, t1, p[i], p[i + 1]);
+              mul2(t2, t3, t2, t3, p[i + 2], p[i + 3]);
+              pk[2 * c4] = pack_bf16(t0, t1);
+              pk[2 * c4 + 1] = pack_bf16(t2, t3);
             }
             tmem_st_x16(tDP + lane_base + col0 + 16 * ch, pk);
           }
@@ -775,7 +844,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(b_dsfull);
-            mbar_arrive(b_qempty(qs));  // this slot's column values are no longer needed
+            mbar_arrive(b_dempty(ds));  // this slot's column values are no longer needed
           }
         }
         if (!ok) break;
