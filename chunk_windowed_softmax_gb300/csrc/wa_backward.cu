@@ -527,7 +527,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = DkvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (C::kSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {  // no room to realign: report, touch nothing
-    if (threadIdx.x == 0) atomicOr(prm.err, kErrBounds);
+    if (threadIdx.x == 0) {
+      atomicOr(prm.err, kErrBounds);
+      ItemFeed{prm.item_counter, prm.n_items, nullptr, 0}.finish();  // keeps the claim counter rewound
+    }
     return;
   }
   const Smem sm = align_smem(smem_raw);
