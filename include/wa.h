@@ -161,7 +161,9 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
  * allocates its backward workspace: B*H*L*4 (rounded up to 256) + 3*B*H*G*n_splits*D*4 bytes, kept until the plan is freed.
  * Errors (synchronous, nothing launched): WA_ERR_INVALID for null or misaligned pointers, or when dq, dk or dv
  * overlaps each other or any input; WA_ERR_OOM when the workspace cannot be allocated; WA_ERR_CUDA when a launch
- * fails. Device-side failures: see wa_plan_check_error().
+ * fails. Device-side failures: see wa_plan_check_error(); besides the wait watchdog, the dk/dv kernel at D = 128
+ * reports WA_ERR_DEVICE_BOUNDS (and computes nothing) if the device gives it a dynamic shared-memory window that is
+ * not 1024-byte aligned, since its buffers leave no room to realign it.
  */
 wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void* v, const void* out, const void* dout,
                       const float* lse, void* dq, void* dk, void* dv, wa_stream_t stream);
