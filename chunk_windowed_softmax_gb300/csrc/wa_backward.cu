@@ -879,39 +879,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   teardown(tmem, warp, feed);
 }
 
-// Dvec_i = dout_i . out_i for every (b, i, h), one warp per row, rows in memory order; fp32 into [B*H][L].
+// Dvec_i = dout_i . out_i for every (b, i, h); fp32 into [B*H][L]. One warp per 8 consecutive rows of one (b, h):
+// each row is read by a group of D/8 lanes with 16-byte loads (all of a warp's loads are issued before any is
+// used), and the warp's 8 results land in one 32-byte sector of dvec.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dot_kernel(const __nv_bfloat16* __restrict__ out,
                                                       const __nv_bfloat16* __restrict__ dout,
-                                                      float* __restrict__ dvec, int64_t rows, int L, int H,
+                                                      float* __restrict__ dvec, int64_t units, int L, int H,
                                                       int64_t sb, int64_t sl, int64_t sh) {
-  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  constexpr int kGroup = D / 8;             // lanes per row: 16 (D = 128) or 8 (D = 64)
+  constexpr int kRowsPerLoad = 32 / kGroup;  // rows covered by one warp-wide load
+  constexpr int kLoads = 8 / kRowsPerLoad;
+  const int64_t u = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // unit: (b, h, block of 8 rows)
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const int h = (int)(r % H);
-  const int64_t bl = r / H;
-  const int l = (int)(bl % L), b = (int)(bl / L);
-  const int64_t off = (int64_t)b * sb + (int64_t)l * sl + (int64_t)h * sh;
-  constexpr int kPer = D / 32;  // elements per lane: 4 (8 bytes) or 2 (4 bytes)
-  float acc = 0.f;
-  if constexpr (kPer == 4) {
-    const uint2 a = __ldg(reinterpret_cast<const uint2*>(out + off) + lane);
-    const uint2 g = __ldg(reinterpret_cast<const uint2*>(dout + off) + lane);
-    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
-    const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
-    const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
-    const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
-    acc = fmaf(a0.x, g0.x, fmaf(a0.y, g0.y, fmaf(a1.x, g1.x, a1.y * g1.y)));
-  } else {
-    const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(out + off) + lane);
-    const uint32_t g = __ldg(reinterpret_cast<const uint32_t*>(dout + off) + lane);
-    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
-    const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g));
-    acc = fmaf(a0.x, g0.x, a0.y * g0.y);
+  if (u >= units) return;
+  const int nlb = (L + 7) / 8;
+  const int64_t bh = u / nlb;
+  const int l0 = (int)(u % nlb) * 8;
+  const int b = (int)(bh / H), h = (int)(bh % H);
+  const int sub = lane % kGroup, grp = lane / kGroup;
+  uint4 a[kLoads], g[kLoads];
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) {
+    const int l = l0 + i * kRowsPerLoad + grp;
+    if (l < L) {
+      const int64_t off = (int64_t)b * sb + (int64_t)l * sl + (int64_t)h * sh + sub * 8;
+      a[i] = __ldg(reinterpret_cast<const uint4*>(out + off));
+      g[i] = __ldg(reinterpret_cast<const uint4*>(dout + off));
+    } else {
+      a[i] = make_uint4(0u, 0u, 0u, 0u);
+      g[i] = a[i];
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) dvec[((int64_t)b * H + h) * L + l] = acc;
+  for (int i = 0; i < kLoads; ++i) {
+    const uint32_t av[4] = {a[i].x, a[i].y, a[i].z, a[i].w}, gv[4] = {g[i].x, g[i].y, g[i].z, g[i].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[e]));
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+#pragma unroll
+    for (int o = kGroup / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    const int l = l0 + i * kRowsPerLoad + grp;
+    if (sub == 0 && l < L) dvec[bh * L + l] = acc;
+  }
 }
 
 // Sum the split partials of the global rows into bf16 rows: tensor blockIdx.y (0 dq, 1 dk, 2 dv), one warp per row,
@@ -963,9 +977,9 @@ int launch_backward_d(const BackwardArgs& a, cudaStream_t s, int num_sms, void* 
   auto rec = [&](int i) { return events ? cudaEventRecord((cudaEvent_t)events[i], s) : cudaSuccess; };
   cudaError_t e = rec(0);
   if (e != cudaSuccess) return (int)e;
-  const int64_t rows = (int64_t)l.B * g.L * l.H;
-  bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
-      reinterpret_cast<const __nv_bfloat16*>(a.out), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.dvec, rows,
+  const int64_t units = (int64_t)l.B * l.H * ((g.L + 7) / 8);
+  bwd_dot_kernel<D><<<(unsigned)((units + 7) / 8), 256, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(a.out), reinterpret_cast<const __nv_bfloat16*>(a.dout), a.dvec, units,
       (int)g.L, l.H, l.stride_b, l.stride_l, l.stride_h);
   if ((e = cudaGetLastError()) != cudaSuccess || (e = rec(1)) != cudaSuccess) return (int)e;
   BwdParams p;
