@@ -2,7 +2,6 @@
 on separate streams; each launch runs the work items whose rows have arrived). Its results must equal the
 device-resident forward bit for bit (the same kernels and work items, only regrouped by launch), and therefore the
 fp64 oracle within the forward's bar."""
-import numpy as np
 import pytest
 import torch
 
