@@ -136,7 +136,8 @@ def test_profile_summaries_parse():
     sys.path.insert(0, root)
     import bench
     for path, key in ((bench.PROFILE_SUMMARY, "dram bytes per full H3 launch"),
-                      (bench.BWD_PROFILE_SUMMARY, "dk/dv dram bytes per full H3 launch")):
+                      (bench.BWD_PROFILE_SUMMARY, "dk/dv dram bytes per full H3 launch"),
+                      (bench.FP8_PROFILE_SUMMARY, "dram bytes per full H3 launch")):
         fields = bench.profile_fields(path)
         assert len(fields["kernel source sha256[:16]"]) == 16
         assert float(fields[key]) > 1e9
