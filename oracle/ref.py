@@ -133,8 +133,9 @@ def window_attention(q, k, v, T, S, K, r, G, global_pos, return_probs=False):
 
 
 def window_attention_rows(q, k, v, T, S, K, r, G, global_pos, b, h, frames=(), global_rows=False):
-    """The same computation restricted to one (b, h) slice and to the listed frames (and the global rows).
+    """The same computation restricted to one (b, h) slice and to the listed frames (and global rows).
 
+    ``global_rows``: False (none), True (all G), or a sequence of global-token numbers g in [0, G) (row g0 + g).
     Rows are independent, so each returned row equals the matching row of ``window_attention``. Returns a dict
     {row index: output row (float64 [D])}. Used to check large workloads on a sample of rows.
     """
@@ -149,9 +150,13 @@ def window_attention_rows(q, k, v, T, S, K, r, G, global_pos, b, h, frames=(), g
         o, _ = attend(_as64(q[b, rows, h]), _as64(k[b, kept, h]), _as64(v[b, kept, h]), scale)
         for i, row in enumerate(rows):
             res[int(row)] = o[i]
-    if global_rows and G:
+    if global_rows is not False and G:
         kept = kept_set_of_global(T, S, G)
-        rows = np.arange(g0, g0 + G, dtype=np.int64)
+        if global_rows is True:
+            rows = np.arange(g0, g0 + G, dtype=np.int64)
+        else:
+            rows = g0 + np.asarray(sorted(set(int(g) for g in global_rows)), dtype=np.int64)
+            assert rows.size == 0 or (rows.min() >= g0 and rows.max() < g0 + G), "global rows lie in [0, G)"
         kk, vv = _as64(k[b, kept, h]), _as64(v[b, kept, h])
         for lo in range(0, G, 256):  # bounded score blocks: G x L may not fit in memory at once
             sel = rows[lo:lo + 256]

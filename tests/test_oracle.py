@@ -359,3 +359,24 @@ def test_planted_mistakes_are_caught(monkeypatch, attr, mutant):
             caught = True
             break
     assert caught, f"planted mistake in {attr} went unnoticed"
+
+
+@pytest.mark.parametrize("gp", [0, 1])
+def test_row_sample_global_subset_matches_full(gp):
+    """A subset of the global rows (numbered 0..G-1 from the first global token) gives exactly those rows, each equal
+    to the full oracle's row; the whole list gives the same rows as global_rows=True."""
+    T, S, K, r, G = 7, 3, 2, 1, 9
+    rng = np.random.default_rng(21 + gp)
+    q, k, v = rand_qkv(rng, 1, T * S + G, 2, 8)
+    full = ref.window_attention(q, k, v, T, S, K, r, G, gp)
+    g0 = ref.global_offset(T, S, gp)
+    sub = [G - 1, 0, 4]
+    got = ref.window_attention_rows(q, k, v, T, S, K, r, G, gp, b=0, h=1, frames=[3], global_rows=sub)
+    assert sorted(got) == sorted(ref.frame_rows(3, S, ref.frame_offset(G, gp)).tolist() + [g0 + g for g in sub])
+    for row, o in got.items():
+        np.testing.assert_allclose(o, full[0, row, 1], atol=1e-13)
+    every = ref.window_attention_rows(q, k, v, T, S, K, r, G, gp, b=0, h=1, global_rows=list(range(G)))
+    alln = ref.window_attention_rows(q, k, v, T, S, K, r, G, gp, b=0, h=1, global_rows=True)
+    assert sorted(every) == sorted(alln) == list(range(g0, g0 + G))
+    for row in every:
+        np.testing.assert_array_equal(every[row], alln[row])

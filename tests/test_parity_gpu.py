@@ -107,28 +107,29 @@ def test_strided_layouts(cuda, kind):
                                         seed=21), strides=kind)
 
 
-def sampled_compare(wa, w, heads, chunks, bench_launch=True):
-    """Full-size workload in the benchmark's launch configuration; the oracle computes a row sample."""
+def sampled_compare(wa, w, heads, chunks, global_rows=True):
+    """Full-size workload in the benchmark's launch configuration; the oracle computes a row sample: every row of
+    the listed chunks of the listed heads, and their global rows (True: all G; or a list of global-token numbers).
+    Only the sampled heads are copied back to the host."""
     dev = torch.device("cuda")
     qd, kd, vd = inputs.make_qkv(w, device=dev)
-    q, k, v = qd.cpu(), kd.cpu(), vd.cpu()
     plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
     try:
         out = plan.forward(qd, kd, vd)
         assert plan.check_error() == 0
-        out_cpu = out.cpu()
+        host = {h: tuple(t[:, :, h:h + 1].cpu() for t in (qd, kd, vd, out)) for h in heads}
     finally:
         plan.close()
     del qd, kd, vd, out
     got, want = {}, {}
-    f0, g0 = w.f0, w.g0
+    frames = [t for c in chunks for t in ref.chunk_frames(c, w.T, w.K)]
     for h in heads:
-        frames = [t for c in chunks for t in ref.chunk_frames(c, w.T, w.K)]
-        res = ref.window_attention_rows(q, k, v, w.T, w.S, w.K, w.r, w.G, w.global_pos, 0, h, frames=frames,
-                                        global_rows=True)
+        q, k, v, o = host[h]
+        res = ref.window_attention_rows(q, k, v, w.T, w.S, w.K, w.r, w.G, w.global_pos, 0, 0, frames=frames,
+                                        global_rows=global_rows)
         rows = sorted(res)
         want[(0, h)] = np.stack([res[r] for r in rows])
-        got[(0, h)] = out_cpu[0, rows, h].float().numpy()
+        got[(0, h)] = o[0, rows, 0].float().numpy()
     return check_slices(got, want, w.name)
 
 
@@ -137,10 +138,17 @@ def test_h3_sampled(cuda):
     sampled_compare(cuda, w, heads=(0, 27, 55), chunks=(0, w.nc // 2, w.nc - 1))
 
 
-@pytest.mark.parametrize("idx", [0, 8, 17])
+SWEEP = configs.sweep()
+
+
+@pytest.mark.parametrize("idx", range(len(SWEEP)), ids=[w.name for w in SWEEP])
 def test_sweep_points_sampled(cuda, idx):
-    w = configs.sweep()[idx]
-    sampled_compare(cuda, w, heads=(0, 55), chunks=(0, w.nc // 2, w.nc - 1))
+    """Every point of the H3-shaped sweep (T in {34, 102}, K in {1, 3, 6}, r in {0, 1, 2}) in the benchmark's
+    launch configuration. Sample: one head per point (a different one for each point), every row of the first,
+    middle and last chunk, and the first and last 128 global rows."""
+    w = SWEEP[idx]
+    sampled_compare(cuda, w, heads=((13 * idx) % w.H,), chunks=(0, w.nc // 2, w.nc - 1),
+                    global_rows=list(range(128)) + list(range(w.G - 128, w.G)))
 
 
 def test_deterministic_and_reusable(cuda):
