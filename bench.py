@@ -187,6 +187,32 @@ def cores_used():
     return n
 
 
+def blas_threads():
+    """The BLAS library numpy's matrix products run on and its live thread count (threadpoolctl when installed,
+    else the getter that numpy's bundled OpenBLAS exports); None when neither can be read."""
+    try:
+        from threadpoolctl import threadpool_info
+        for i in threadpool_info():
+            if i.get("user_api") == "blas":
+                return {"library": i.get("internal_api"), "threads": i.get("num_threads")}
+    except Exception:
+        pass
+    import ctypes
+    import glob
+    import numpy
+    d = os.path.dirname(numpy.__file__)
+    for lib in sorted(glob.glob(os.path.join(d, "..", "numpy.libs", "*openblas*")) +
+                      glob.glob(os.path.join(d, ".libs", "*openblas*"))):
+        try:
+            handle = ctypes.CDLL(lib)
+        except OSError:
+            continue
+        for fn in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            if hasattr(handle, fn):
+                return {"library": os.path.basename(lib), "threads": int(getattr(handle, fn)())}
+    return None
+
+
 def run_reference(args, w, rank):
     """The CPU oracle, as it stands, on the host cores: each step a bounded row sample of the workload."""
     if rank != 0:
@@ -216,7 +242,7 @@ def run_reference(args, w, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w, {"timed": "CPU oracle (numpy float64) on a row sample per step"}),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "blas": blas_threads()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -487,6 +513,7 @@ def main():
         chunks = sorted({0, nc // 2, nc - 1})
         s, f, nrows = oracle_sample(w, qc, kc, vc, heads, chunks, global_rows=True)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+               "blas": blas_threads(),
                "sample": f"heads {heads}: all {w.G} global rows + every row of chunks {chunks} ({nrows} rows, "
                          f"{f / 1e12:.3f} kept TFLOP, {s:.1f} s); throughput of the sample"}
 

@@ -354,9 +354,10 @@ class Plan:
 def forward(q, k, v, T, S, K, r, G, global_pos=0, out=None):
     """One-shot call: out = window attention of q, k, v ([B, L, H, D] bf16 on a CUDA device).
 
-    CPU tensors are accepted too (end-to-end use): wa_forward_host copies them to the current CUDA device in head
-    groups, overlapping the copies with the computation (pinned tensors let the copies run asynchronously), and
-    writes the result into a CPU tensor.
+    CPU tensors are accepted too (end-to-end use): wa_forward_host copies them to the current CUDA device in pieces
+    of sequence rows (the global rows first, then the frames one window group at a time), runs the work items whose
+    rows have arrived while later pieces are still being copied (pinned tensors let the copies run asynchronously),
+    and copies each finished block of the result back into a CPU tensor.
     """
     B, L, H, D = q.shape
     plan = Plan(T, S, K, r, G, B, H, D, global_pos, strides=tuple(q.stride()[:3]))

@@ -150,7 +150,9 @@ struct EpiCols {
 //                          group per thread
 //   warp 4 kCG            MMA issuer X (whole warp, one elected lane issues): S = Q K^T and dq += dS K
 //   warp 4 kCG + 1        MMA issuer Y (whole warp, one elected lane issues): dP = dout V^T
-//   warp 4 kCG + 2        TMA producer (one thread): Q and dout tiles of the sub-item, rings of key and value tiles
+//   warp 4 kCG + 2        TMA producer (whole warp; lane 0 claims items and issues the copies): Q and dout tiles of
+//                          the sub-item, rings of key and value tiles; the lanes zero the rows of a segment's last key
+//                          tile that lie past the segment's end before releasing it
 // TMEM: R0, R1 [0,256) score buffers (step n's S in R[n % 2]; dS, packed bf16, overwrites the front of each group's
 // columns and is the A operand of dS.K straight from TMEM), R2 [256,384) dP, R3 [384, 384+D) the dq accumulator.
 // The next step's S and dP are issued before this step's dS.K, so the elementwise work of a step overlaps the
@@ -165,8 +167,9 @@ struct DqCfg {
   static constexpr int kVOff = kKOff + kKSlots * kTileBytes;
   static constexpr int kBarOff = kVOff + kVSlots * kTileBytes;
   // q_full, q_empty, s_full[2], p_full[2], dp_free, o_full, drain_x, drain_y, then the rings' full / empty barriers,
-  // then the work-item ring's (ItemFeed)
-  static constexpr int kNumBars = 10 + 2 * kKSlots + 2 * kVSlots + 2 * kItemRingSlots;
+  // k_land (a segment's last key tile lands there and is cleaned before its full barrier is arrived), then the
+  // work-item ring's (ItemFeed)
+  static constexpr int kNumBars = 10 + 2 * kKSlots + 2 * kVSlots + 1 + 2 * kItemRingSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
   static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kItemRingSlots + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -175,7 +178,7 @@ struct DqCfg {
 };
 
 // dS = P (dP - Dvec) for one thread's kCW columns of one row, packed to bf16 over the front of those columns.
-// kMask: columns at or past `valid` (a segment's ragged last tile) get P = 0.
+// kMask: columns at or past `valid` (a segment's ragged last tile) get dS = 0.
 template <bool kMask>
 __device__ __forceinline__ void dq_row_step(uint32_t tS, const uint32_t (&dpr)[kCW / 32][32], float c_log2,
                                             float neg_lse2, float drow, int col0, int valid) {
@@ -187,15 +190,15 @@ __device__ __forceinline__ void dq_row_step(uint32_t tS, const uint32_t (&dpr)[k
     for (int c = 0; c < 16; ++c) {  // packed pairs: one f32x2 instruction per two columns
       float x0, x1, t0, t1, d0, d1;
       fma2(x0, x1, __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]), c_log2, c_log2, neg_lse2, neg_lse2);
-      float p0 = ex2(x0);
-      float p1 = ex2(x1);
-      if (kMask) {
-        const int col = col0 + 32 * ch + 2 * c;
-        p0 = col < valid ? p0 : 0.f;
-        p1 = col + 1 < valid ? p1 : 0.f;
-      }
+      const float p0 = ex2(x0);
+      const float p1 = ex2(x1);
       add2(t0, t1, __uint_as_float(dpr[ch][2 * c]), __uint_as_float(dpr[ch][2 * c + 1]), -drow, -drow);
       mul2(d0, d1, p0, p1, t0, t1);
+      if (kMask) {  // selected, not multiplied: dP there comes from value rows outside the segment (maybe not finite)
+        const int col = col0 + 32 * ch + 2 * c;
+        d0 = col < valid ? d0 : 0.f;
+        d1 = col + 1 < valid ? d1 : 0.f;
+      }
       pk[c] = pack_bf16(d0, d1);
     }
     tmem_st_x16(tS + 16 * ch, pk);
@@ -220,6 +223,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto b_kempty = [&](uint32_t s) { return bar + 8 * (10 + C::kKSlots + s); };
   auto b_vfull = [&](uint32_t s) { return bar + 8 * (10 + 2 * C::kKSlots + s); };
   auto b_vempty = [&](uint32_t s) { return bar + 8 * (10 + 2 * C::kKSlots + C::kVSlots + s); };
+  const uint32_t b_kland = bar + 8 * (10 + 2 * C::kKSlots + 2 * C::kVSlots);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
   const ItemFeed feed{prm.item_counter, prm.n_items, reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 16),
@@ -247,6 +251,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_vfull(s), 1);
       mbar_init(b_vempty(s), 1);
     }
+    mbar_init(b_kland, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -262,11 +267,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == kLoadWarp) {
     // ---------------------------------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      uint32_t k_n = 0, v_n = 0, q_n = 0;
+    // The whole warp runs the loop (waits are warp-wide); lane 0 claims the items and issues the copies. A
+    // segment's last key tile lands on k_land: the 32 lanes zero its rows past the segment's end (keys outside the
+    // rows' kept sets: their dS is 0, but 0 x Inf would be NaN in dS.K) before k_full is arrived.
+    {
+      const bool leader = lane == 0;
+      uint32_t k_n = 0, v_n = 0, q_n = 0, kl_n = 0;  // kl_n: segment-final key tiles landed on k_land
       bool ok = true, dropped = false;
       for (uint32_t n = 0; ok; ++n) {
-        const int idx = feed.claim(n, abort_flag, err, ok);
+        const int idx = feed.claim_warp(n, abort_flag, err, ok);
         if (idx < 0) break;
         const Item it = load_item(prm.items, idx);
         const int b = it.bh / prm.H, h = it.bh % prm.H;
@@ -274,38 +283,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
         const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
         for (int t = 0; t < ntq && ok; ++t) {
-          ok = mbar_wait(b_qempty, (q_n & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = mbar_wait_warp(b_qempty, (q_n & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           if (!ok) break;
-          if ((prm.debug_flags & 2) && !dropped && blockIdx.x == 0) {
-            dropped = true;  // fault injection for the watchdog test: this sub-item's query tiles never arrive
-          } else {
-            mbar_arrive_expect_tx(b_qfull, 2 * C::kTileBytes);
-            load_tile<D>(sQ, &tm_q, b_qfull, h, it.q_lo + t * kTileRows, b);
-            load_tile<D>(sDO, &tm_do, b_qfull, h, it.q_lo + t * kTileRows, b);
+          if (leader) {
+            if ((prm.debug_flags & 2) && !dropped && blockIdx.x == 0) {
+              dropped = true;  // fault injection for the watchdog test: this sub-item's query tiles never arrive
+            } else {
+              mbar_arrive_expect_tx(b_qfull, 2 * C::kTileBytes);
+              load_tile<D>(sQ, &tm_q, b_qfull, h, it.q_lo + t * kTileRows, b);
+              load_tile<D>(sDO, &tm_do, b_qfull, h, it.q_lo + t * kTileRows, b);
+            }
           }
           q_n++;
           for (int j = 0; j < nt && ok; ++j) {
             int valid;
             const int row = step_row(it, j, nt0, &valid);
+            const bool tail = valid < kTileRows;
             const uint32_t ks = k_n % C::kKSlots, vs = v_n % C::kVSlots;
-            ok = mbar_wait(b_kempty(ks), ((k_n / C::kKSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            ok = mbar_wait_warp(b_kempty(ks), ((k_n / C::kKSlots) & 1) ^ 1, abort_flag, err, kErrTimeout,
+                                kWaitLimitNs);
             if (!ok) break;
-            mbar_arrive_expect_tx(b_kfull(ks), C::kTileBytes);
-            load_tile<D>(sK + ks * C::kTileBytes, &tm_k, b_kfull(ks), h, row, b);
+            if (leader) {
+              const uint32_t kbar = tail ? b_kland : b_kfull(ks);
+              mbar_arrive_expect_tx(kbar, C::kTileBytes);
+              load_tile<D>(sK + ks * C::kTileBytes, &tm_k, kbar, h, row, b);
+            }
             k_n++;
-            ok = mbar_wait(b_vempty(vs), ((v_n / C::kVSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-            if (!ok) break;
-            mbar_arrive_expect_tx(b_vfull(vs), C::kTileBytes);
-            load_tile<D>(sV + vs * C::kTileBytes, &tm_v, b_vfull(vs), h, row, b);
-            v_n++;
+            ok = mbar_wait_warp(b_vempty(vs), ((v_n / C::kVSlots) & 1) ^ 1, abort_flag, err, kErrTimeout,
+                                kWaitLimitNs);
+            if (ok && leader) {
+              mbar_arrive_expect_tx(b_vfull(vs), C::kTileBytes);
+              load_tile<D>(sV + vs * C::kTileBytes, &tm_v, b_vfull(vs), h, row, b);
+            }
+            if (ok) v_n++;
+            if (tail) {  // the value copy is already on its way; now clean the key tile and release it
+              const bool landed = mbar_wait_warp(b_kland, kl_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              kl_n++;
+              if (landed) zero_tile_rows(sK + ks * C::kTileBytes, D / 64, valid, lane);
+              if (leader) mbar_arrive(b_kfull(ks));  // in place of the copy's arrival (also when unwinding)
+              ok = ok && landed;
+            }
           }
         }
       }
-      if (!ok) {  // let the copies already issued land before the CTA's shared memory goes away
+      if (!ok && leader) {  // let the copies already issued land before the CTA's shared memory goes away
         for (uint32_t n = k_n > (uint32_t)C::kKSlots ? k_n - C::kKSlots : 0; n < k_n; ++n)
           mbar_wait_drain(b_kfull(n % C::kKSlots), (n / C::kKSlots) & 1, kDrainLimitNs);
         for (uint32_t n = v_n > (uint32_t)C::kVSlots ? v_n - C::kVSlots : 0; n < v_n; ++n)
           mbar_wait_drain(b_vfull(n % C::kVSlots), (n / C::kVSlots) & 1, kDrainLimitNs);
+        if (kl_n) mbar_wait_drain(b_kland, (kl_n - 1) & 1, kDrainLimitNs);
         if (q_n) mbar_wait_drain(b_qfull, (q_n - 1) & 1, kDrainLimitNs);
       }
     }
@@ -479,11 +505,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //                          -> bf16 into TMEM. P stays in fp32 registers between the phases.
 //   warp 4 kCG            MMA issuer: S^T = K Q^T, dP^T = V dout^T, dv += P^T dout, dk += dS^T Q
 //   warp 4 kCG + 1        query-tile loader (the dq kernel's second issuer; both kernels share one launch shape):
-//                          lane 0 issues the TMA copies of the query tiles into their own ring
+//                          lane 0 issues the TMA copies of the query tiles into their own ring; the lanes zero the
+//                          rows of a segment's last tile that lie past the segment's end before releasing it
 //   warp 4 kCG + 2        loads (all lanes): lane 0 issues the TMA copies (the key / value tiles of the sub-item and
 //                          a ring of dout tiles); every lane then stages 4 query columns' values (log2-domain lse,
 //                          Dvec, both negated) into the dout slot. Columns past the segment get -lse' = -inf and
-//                          -Dvec = 0, so their P and dS are exactly 0 with no masking in the elementwise code.
+//                          -Dvec = 0, and (as for the query tiles) the rows of a segment's last dout tile past the
+//                          segment's end are zeroed before release, so their P and dS are exactly 0 and every
+//                          product with them is 0, with no masking in the elementwise code.
 // TMEM: S^T [0,128) (P^T packed over the front of each group's columns), dP^T [128,256) (dS^T likewise),
 // dv [256, 256+D), dk [384, 384+D). Issue order per step n: dv(n) after P^T(n) is written, then S^T(n+1); dk(n)
 // after dS^T(n), then dP^T(n+1). So the tensor core computes dv(n) and S^T(n+1) while the elementwise warps work on
@@ -506,13 +535,15 @@ struct DkvCfg {
   static constexpr int kColBytes = 64 * 16;
   static constexpr int kBarOff = kColOff + kDSlots * kColBytes;
   // kv_full, kv_empty, s_full, p_full, dp_full, ds_full, o_full, drain_x, q_full[], q_empty[], d_full[], d_empty[],
-  // then the ItemFeed's 2 kItemRingSlots
-  static constexpr int kNumBars = 8 + 2 * kQSlots + 2 * kDSlots + 2 * kItemRingSlots;
+  // q_land, d_land (a segment's last query / dout tile lands there and is cleaned before its full barrier is
+  // arrived), then the ItemFeed's 2 kItemRingSlots
+  static constexpr int kNumBars = 8 + 2 * kQSlots + 2 * kDSlots + 2 + 2 * kItemRingSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
   static constexpr int kUsed = kMiscOff + 16 + 4 * kItemRingSlots;
-  // Room to realign the window to 1024 bytes where it fits; otherwise the window itself must be aligned (checked
-  // at launch).
-  static constexpr int kSlack = kUsed + 1024 <= 232448 ? 1024 : 0;
+  // Room to realign the window to 1024 bytes (the 128-byte swizzle repeats every 1024 bytes): a full 1024 where it
+  // fits, else what is left of the 227 KB (D = 128: 768 bytes, so any window on a 256-byte boundary still works).
+  // A window further off than that is reported at launch (WA_ERR_DEVICE_BOUNDS) and nothing is computed.
+  static constexpr int kSlack = kUsed + 1024 <= 232448 ? 1024 : (232448 - kUsed) / 16 * 16;
   static constexpr int kSmemBytes = kUsed + kSlack;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
@@ -526,7 +557,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    const BwdParams prm) {
   using C = DkvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  if (C::kSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {  // no room to realign: report, touch nothing
+  if (((0u - smem_u32(smem_raw)) & 1023u) > (uint32_t)C::kSlack) {  // no room to realign: report, touch nothing
     if (threadIdx.x == 0) {
       atomicOr(prm.err, kErrBounds);
       ItemFeed{prm.item_counter, prm.n_items, nullptr, 0}.finish();  // keeps the claim counter rewound
@@ -543,6 +574,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto b_qempty = [&](uint32_t s) { return bar + 8 * (8 + C::kQSlots + s); };
   auto b_dfull = [&](uint32_t s) { return bar + 8 * (8 + 2 * C::kQSlots + s); };
   auto b_dempty = [&](uint32_t s) { return bar + 8 * (8 + 2 * C::kQSlots + C::kDSlots + s); };
+  const uint32_t b_qland = bar + 8 * (8 + 2 * C::kQSlots + 2 * C::kDSlots);
+  const uint32_t b_dland = b_qland + 8;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm.p + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 4);
   const ItemFeed feed{prm.item_counter, prm.n_items, reinterpret_cast<volatile int*>(sm.p + C::kMiscOff + 16),
@@ -567,6 +600,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_dfull(s), 1 + 32);         // the copy's expect-tx arrival + one per loader lane (column values)
       mbar_init(b_dempty(s), 1 + kEwWarps);  // the MMA commit after dv(j) + one per elementwise warp
     }
+    mbar_init(b_qland, 1);
+    mbar_init(b_dland, 1);
     feed.init(kEwWarps + 2);  // item consumers: the issuer, the query-tile loader, the elementwise warps
     *abort_flag = 0;
     fence_mbar_init();
@@ -583,7 +618,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == kLoadWarp) {
     // ---------------------------------------------------------------- key/value, dout and column-value loader
-    uint32_t kv_n = 0, d_n = 0;
+    uint32_t kv_n = 0, d_n = 0, dl_n = 0;  // dl_n: segment-final dout tiles landed on d_land
     bool ok = true, dropped = false;
     for (uint32_t n = 0; ok; ++n) {
       const int idx = feed.claim_warp(n, abort_flag, err, ok);
@@ -620,16 +655,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = mbar_wait(b_dempty(ds), ((d_n / C::kDSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
+          // A segment's last tile lands on d_land: its rows past the segment's end (queries that do not keep these
+          // keys) are zeroed before d_full is arrived, so every product with them is exactly 0 (their P and dS are
+          // 0: -lse' = -inf and -Dvec = 0 below), whatever those rows hold.
+          const bool tail = valid < kTileRows;
           if (lane == 0) {
-            mbar_arrive_expect_tx(b_dfull(ds), C::kTileBytes);
+            const uint32_t dbar = tail ? b_dland : b_dfull(ds);
+            mbar_arrive_expect_tx(dbar, C::kTileBytes);
             if ((prm.debug_flags & 4) && !dropped && blockIdx.x == 0)
               dropped = true;  // fault injection for the watchdog test: bytes expected, no copy issued
             else
-              load_tile<D>(sDO + ds * C::kTileBytes, &tm_do, b_dfull(ds), h, row, b);
+              load_tile<D>(sDO + ds * C::kTileBytes, &tm_do, dbar, h, row, b);
           }
           const uint32_t cb = sCol + ds * C::kColBytes + 16 * lane;
           sts_f4(cb, make_float4(l4[0], l4[1], l4[2], l4[3]));
           sts_f4(cb + 512, make_float4(d4[0], d4[1], d4[2], d4[3]));
+          if (tail) {
+            ok = mbar_wait(b_dland, dl_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            dl_n++;
+            if (ok) zero_tile_rows(sDO + ds * C::kTileBytes, D / 64, valid, lane);
+            if (lane == 0) mbar_arrive(b_dfull(ds));  // in place of the copy's arrival
+          }
           mbar_arrive(b_dfull(ds));  // release: the column values are visible to whoever waits on d_full
           d_n++;
         }
@@ -637,12 +684,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (!ok && lane == 0) {
       if (kv_n) mbar_wait_drain(b_kvfull, (kv_n - 1) & 1, kDrainLimitNs);
+      if (dl_n) mbar_wait_drain(b_dland, (dl_n - 1) & 1, kDrainLimitNs);
       for (uint32_t n = d_n > (uint32_t)C::kDSlots ? d_n - C::kDSlots : 0; n < d_n; ++n)
         mbar_wait_drain(b_dfull(n % C::kDSlots), (n / C::kDSlots) & 1, kDrainLimitNs);
     }
   } else if (warp == kMmaWarpY) {
     // ------------------------------------------------------------------------------------- query-tile loader
-    uint32_t q_n = 0;
+    uint32_t q_n = 0, ql_n = 0;  // ql_n: segment-final query tiles landed on q_land
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
       const int idx = feed.fetch(n, abort_flag, err, ok);
@@ -660,17 +708,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = mbar_wait(b_qempty(qs), ((q_n / C::kQSlots) & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
+          // a segment's last tile: cleaned like the dout tiles (rows past the segment's end become zeros)
+          const bool tail = valid < kTileRows;
           if (lane == 0) {
-            mbar_arrive_expect_tx(b_qfull(qs), C::kTileBytes);
-            load_tile<D>(sQ + qs * C::kTileBytes, &tm_q, b_qfull(qs), h, row, b);
+            const uint32_t qbar = tail ? b_qland : b_qfull(qs);
+            mbar_arrive_expect_tx(qbar, C::kTileBytes);
+            load_tile<D>(sQ + qs * C::kTileBytes, &tm_q, qbar, h, row, b);
           }
           q_n++;
+          if (tail) {
+            ok = mbar_wait(b_qland, ql_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            ql_n++;
+            if (ok) zero_tile_rows(sQ + qs * C::kTileBytes, D / 64, valid, lane);
+            if (lane == 0) mbar_arrive(b_qfull(qs));  // in place of the copy's arrival
+          }
         }
       }
     }
     if (!ok && lane == 0) {
       for (uint32_t n = q_n > (uint32_t)C::kQSlots ? q_n - C::kQSlots : 0; n < q_n; ++n)
         mbar_wait_drain(b_qfull(n % C::kQSlots), (n / C::kQSlots) & 1, kDrainLimitNs);
+      if (ql_n) mbar_wait_drain(b_qland, (ql_n - 1) & 1, kDrainLimitNs);
     }
   } else if (warp == kMmaWarpX) {
     // ------------------------------------------------------------------------------------------ MMA issuer
@@ -958,16 +1017,8 @@ __global__ void __launch_bounds__(256) bwd_sum_kernel(const float* __restrict__ 
 
 template <int D>
 int launch_backward_d(const BackwardArgs& a, cudaStream_t s, int num_sms, void* const* events) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(wa_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DqCfg<D>::kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(wa_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               DkvCfg<D>::kSmemBytes);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  if (int e = ensure_smem_attr(reinterpret_cast<const void*>(&wa_dq_kernel<D>), DqCfg<D>::kSmemBytes)) return e;
+  if (int e = ensure_smem_attr(reinterpret_cast<const void*>(&wa_dkdv_kernel<D>), DkvCfg<D>::kSmemBytes)) return e;
   const Geometry& g = *a.geo;
   const wa_layout_t& l = g.layout;
   alignas(64) CUtensorMap mq, mk, mv, mdo;

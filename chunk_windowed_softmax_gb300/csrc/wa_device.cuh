@@ -23,6 +23,30 @@ __device__ __forceinline__ Item load_item(const Item* items, int idx) {
 // Number of 128-row tiles of the half-open row range [lo, hi).
 __device__ __forceinline__ int seg_tiles(int lo, int hi) { return hi > lo ? (hi - lo + kTileRows - 1) / kTileRows : 0; }
 
+// Rows of the j-th 128-row tile of an item's key segments that lie inside the segment (128 except in a segment's
+// last tile); nt0 = seg_tiles of segment 0.
+__device__ __forceinline__ int tile_valid(const Item& it, int j, int nt0) {
+  return j < nt0 ? min(kTileRows, it.s0_hi - (it.s0_lo + j * kTileRows))
+                 : min(kTileRows, it.s1_hi - (it.s1_lo + (j - nt0) * kTileRows));
+}
+
+// Zero rows [valid, 128) of a 128-row tile held in shared memory as `boxes` consecutive boxes of 128 rows x 128
+// bytes (a row of a box is 128 contiguous bytes, so the 128-byte swizzle inside a row does not matter). A segment's
+// last tile is copied whole and so holds rows past the segment's end: tokens outside the rows' kept sets, or past
+// the sequence (zero-filled by the copy). Their scores or probabilities are masked to zero, but a tensor-core
+// product of zero with an Inf or NaN there would still be NaN; zeroing the rows keeps every result independent of
+// tokens outside its kept set. Called by all 32 lanes of a warp after the tile's copy has completed; the writes are
+// fenced for the tensor core's (async-proxy) reads and the warp is reconverged before it returns.
+__device__ __forceinline__ void zero_tile_rows(uint32_t tile, int boxes, int valid, int lane) {
+  const uint32_t chunks = (uint32_t)(kTileRows - valid) * 8;  // 16-byte chunks per box
+  for (int hf = 0; hf < boxes; ++hf) {
+    const uint32_t base = tile + (uint32_t)(hf * kTileRows * 128 + valid * 128);
+    for (uint32_t c = lane; c < chunks; c += 32) ptx::sts_u4(base + 16 * c, 0u, 0u, 0u, 0u);
+  }
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // Hand-out of the work items of a persistent launch to its CTAs. Without a counter, CTA c runs the items c,
 // c + grid, c + 2 grid, ... With a counter (two device ints, zero when the launch starts: items claimed so far and
 // CTAs finished), one producer thread of each CTA claims the next unclaimed item when it is ready for one, so CTAs

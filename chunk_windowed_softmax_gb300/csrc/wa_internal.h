@@ -117,6 +117,15 @@ struct BackwardArgs {
 // holds five CUDA events recorded before, between and after the four launches. Returns a CUDA error code.
 int launch_backward(const BackwardArgs& a, void* stream, int num_sms, void* const* events);
 
+// Identity of the CUDA context current on the calling thread (the driver's context id: unique for the life of the
+// process, so a context created after cudaDeviceReset gets a new one). Makes the device's primary context current
+// first when the runtime has not yet done so. Returns 0 when it cannot be read.
+unsigned long long current_context_id();
+// Opt `func` into `bytes` of dynamic shared memory in the current context, once per (kernel, context): the
+// attribute belongs to the context, so a second device (or a context rebuilt after a reset) needs its own call.
+// Thread-safe. Returns a CUDA error code (0 on success).
+int ensure_smem_attr(const void* func, int bytes);
+
 // Encode the 4-D TMA map of a [B, L, H, D] tensor (box 128 bytes x 1 x 128 rows x 1, 128-byte swizzle) into
 // `map` (a 64-byte aligned CUtensorMap). elem_bytes 2: bf16, 1: 8-bit. Returns false if encoding fails.
 bool make_tile_map(void* map, const void* ptr, const Geometry& g, int elem_bytes);

@@ -11,9 +11,13 @@
 //   warps 4-7   softmax warpgroup of query tile 1
 //   warp 8      MMA issuer: S_t = Q_t K^T and O_t += P_t V with tcgen05.mma, accumulators in TMEM; the whole warp
 //               runs the loop and one elect.sync-chosen lane issues (the issue model in wa_ptx.cuh)
-//   warp 9      TMA producer (one thread): Q tiles and rings of K / V tiles, 128-byte swizzled; each step's K_j and
-//               V_{j-1} complete on one bundle barrier. It also claims the CTA's next work item from a global
-//               counter when it is ready for one, and passes the index to the other roles through a shared ring
+//   warp 9      TMA producer (the whole warp runs the loop, lane 0 issues): Q tiles and rings of K / V tiles,
+//               128-byte swizzled; each step's K_j and V_{j-1} complete on one bundle barrier. It also claims the
+//               CTA's next work item from a global counter when it is ready for one, and passes the index to the
+//               other roles through a shared ring. A segment's last V tile lands on a barrier of its own first:
+//               the 32 lanes zero its rows past the segment's end (tokens outside the rows' kept sets, where P is 0
+//               but 0 x Inf would be NaN) and only then release the bundle, so the MMA and softmax roles never
+//               see a ragged tail
 //   warps 10-11 idle
 // Full window tiles (D = 128) leave through a shared-memory stage and TMA stores; the rest is stored directly.
 // The launch gives every thread 168 registers (384 x 168 = 64512); setmaxnreg then moves them to where the work
@@ -85,8 +89,8 @@ struct Cfg {
   static constexpr int kStageOff = kVOff + kVSlots * kVTileBytes;
   static constexpr int kBarOff = kStageOff + (kStage ? 2 * kStageTileBytes : 0);
   // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain b_full[kLag] b_empty[kLag]
-  //           item ring full[kItemRingSlots] empty[kItemRingSlots]  stage_full[2] stage_free[2]
-  static constexpr int kNumBars = 11 + 2 * kLag + 2 * kItemRingSlots + 4;
+  //           item ring full[kItemRingSlots] empty[kItemRingSlots]  stage_full[2] stage_free[2] v_land
+  static constexpr int kNumBars = 11 + 2 * kLag + 2 * kItemRingSlots + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
   static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kItemRingSlots + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t kTmemO = 256;
@@ -134,6 +138,8 @@ struct BarAddr {
   __device__ __forceinline__ uint32_t stage_free(int t) const {
     return base + 8 * (13 + 2 * NB + 2 * kItemRingSlots + t);
   }
+  // a segment's last V tile lands here (not on its bundle's barrier) so the producer can clean it first
+  __device__ __forceinline__ uint32_t v_land() const { return base + 8 * (15 + 2 * NB + 2 * kItemRingSlots); }
 };
 
 // Exponentiate one 128-column score row into bf16 P (written to TMEM over the row's S columns, 16 columns per
@@ -200,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.stage_full(t), 4);  // one arrive per warp of the tile's warpgroup
       mbar_init(bars.stage_free(t), 1);  // the store issuer, once the copy engine has read the stage
     }
+    mbar_init(bars.v_land(), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -233,13 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kControlRegs>();
     if (warp == kLoadWarp) {
     // ------------------------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop (waits are warp-wide); lane 0 claims the items and issues the copies.
+    {
+      const bool leader = lane == 0;
       uint32_t k_n = 0, v_n = 0, b_n = 0;  // K tiles, V tiles and step bundles loaded so far
+      uint32_t vt_n = 0;                   // segment-final V tiles landed on v_land so far
       uint32_t q_n0 = 0, q_n1 = 0;
       bool dropped = false;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n) {
-        const int idx = feed.claim(n, abort_flag, err, ok);
+        const int idx = feed.claim_warp(n, abort_flag, err, ok);
         if (idx < 0) break;
         const Item it = load_item(prm.items, idx);
         const int b = it.bh / prm.H, h = it.bh % prm.H;
@@ -248,13 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           if (t >= ntq || !ok) break;
           uint32_t& qn = t ? q_n1 : q_n0;
-          ok = mbar_wait(bars.q_empty(t), (qn & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = mbar_wait_warp(bars.q_empty(t), (qn & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
           if (!ok) break;
-          mbar_arrive_expect_tx(bars.q_full(t), C::kQTileBytes);
+          if (leader) {
+            mbar_arrive_expect_tx(bars.q_full(t), C::kQTileBytes);
 #pragma unroll
-          for (int hf = 0; hf < C::kQKBoxes; ++hf)
-            tma_load_4d(sQ + t * C::kQTileBytes + hf * C::kBoxBytes, &tmap_q, bars.q_full(t), hf * C::kQKBoxElems,
-                        h, it.q_lo + t * kTileRows, b);
+            for (int hf = 0; hf < C::kQKBoxes; ++hf)
+              tma_load_4d(sQ + t * C::kQTileBytes + hf * C::kBoxBytes, &tmap_q, bars.q_full(t), hf * C::kQKBoxElems,
+                          h, it.q_lo + t * kTileRows, b);
+          }
           qn++;
         }
         const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
@@ -264,36 +276,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j <= nt && ok; ++j) {
           if (b_n >= (uint32_t)C::kLag) {
             const uint32_t w = b_n - C::kLag;
-            ok = mbar_wait(bars.b_empty(w), (w / C::kLag) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            ok = mbar_wait_warp(bars.b_empty(w), (w / C::kLag) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
             if (!ok) break;
           }
           const uint32_t full = bars.b_full(b_n);
-          mbar_arrive_expect_tx(full, (j < nt ? C::kQTileBytes : 0) + (j >= 1 ? C::kVTileBytes : 0));
-          if ((prm.debug_flags & 1) && !dropped && blockIdx.x == 0 && j < nt) {
-            dropped = true;  // fault injection for the watchdog test: this key tile is never loaded
-          } else if (j < nt) {
-            const uint32_t slot = k_n % C::kKSlots;
+          const uint32_t kbytes = j < nt ? C::kQTileBytes : 0;
+          // V_{j-1} ends a segment mid-tile: it lands on v_land and the bundle is released after the cleaning below
+          const int vvalid = j >= 1 ? tile_valid(it, j - 1, nt0) : kTileRows;
+          const bool vtail = vvalid < kTileRows;
+          const uint32_t vslot = v_n % C::kVSlots;
+          if (leader) {
+            if (vtail) {
+              mbar_expect_tx(full, kbytes);  // the pending arrival is made once the V tile is clean
+              mbar_arrive_expect_tx(bars.v_land(), C::kVTileBytes);
+            } else {
+              mbar_arrive_expect_tx(full, kbytes + (j >= 1 ? C::kVTileBytes : 0));
+            }
+            if ((prm.debug_flags & 1) && !dropped && blockIdx.x == 0 && j < nt) {
+              dropped = true;  // fault injection for the watchdog test: this key tile is never loaded
+            } else if (j < nt) {
+              const uint32_t slot = k_n % C::kKSlots;
 #pragma unroll
-            for (int hf = 0; hf < C::kQKBoxes; ++hf)
-              tma_load_4d(sK + slot * C::kQTileBytes + hf * C::kBoxBytes, &tmap_k, full, hf * C::kQKBoxElems, h,
-                          row_of(j), b);
-          }
-          if (j >= 1) {
-            const uint32_t slot = v_n % C::kVSlots;
+              for (int hf = 0; hf < C::kQKBoxes; ++hf)
+                tma_load_4d(sK + slot * C::kQTileBytes + hf * C::kBoxBytes, &tmap_k, full, hf * C::kQKBoxElems, h,
+                            row_of(j), b);
+            }
+            if (j >= 1) {
+              const uint32_t vbar = vtail ? bars.v_land() : full;
 #pragma unroll
-            for (int hf = 0; hf < C::kVBoxes; ++hf)
-              tma_load_4d(sV + slot * C::kVTileBytes + hf * C::kBoxBytes, &tmap_v, full, hf * 64, h, row_of(j - 1),
-                          b);
+              for (int hf = 0; hf < C::kVBoxes; ++hf)
+                tma_load_4d(sV + vslot * C::kVTileBytes + hf * C::kBoxBytes, &tmap_v, vbar, hf * 64, h,
+                            row_of(j - 1), b);
+            }
           }
           if (j < nt) k_n++;
           if (j >= 1) v_n++;
           b_n++;
+          if (vtail) {
+            ok = mbar_wait_warp(bars.v_land(), vt_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            vt_n++;
+            if (ok) zero_tile_rows(sV + vslot * C::kVTileBytes, C::kVBoxes, vvalid, lane);
+            if (leader) mbar_arrive(full);  // release the bundle (also when unwinding, so that it can drain)
+          }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // Unwinding: wait (briefly) for the copies still in flight so that none lands after the CTA exits.
         for (uint32_t n = b_n > (uint32_t)C::kLag ? b_n - C::kLag : 0; n < b_n; ++n)
           mbar_wait_drain(bars.b_full(n), (n / C::kLag) & 1, kDrainLimitNs);
+        if (vt_n) mbar_wait_drain(bars.v_land(), (vt_n - 1) & 1, kDrainLimitNs);
         if (q_n0) mbar_wait_drain(bars.q_full(0), (q_n0 - 1) & 1, kDrainLimitNs);
         if (q_n1) mbar_wait_drain(bars.q_full(1), (q_n1 - 1) & 1, kDrainLimitNs);
       }
@@ -410,8 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j) {
-        const int valid = j < nt0 ? min(kTileRows, it.s0_hi - (it.s0_lo + j * kTileRows))
-                                  : min(kTileRows, it.s1_hi - (it.s1_lo + (j - nt0) * kTileRows));
+        const int valid = tile_valid(it, j, nt0);
         ok = mbar_wait(bar_s, s_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         s_n++;
@@ -603,15 +633,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // Looked up once, by a thread-safe static initialisation (the driver entry point is the same in every context).
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cudaGetLastError();
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -635,13 +667,8 @@ bool make_map(CUtensorMap* m, const void* ptr, const Geometry& g, int elem_bytes
 template <int D, bool kF8>
 int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
   using C = Cfg<D, kF8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<D, kF8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  if (int e = ensure_smem_attr(reinterpret_cast<const void*>(&window_attention_kernel<D, kF8>), C::kSmemBytes))
+    return e;
   CUtensorMap mq, mk, mv, mo;
   const int qk_bytes = kF8 ? 1 : 2;
   if (!make_map(&mq, a.q, *a.geo, qk_bytes) || !make_map(&mk, a.k, *a.geo, qk_bytes) ||

@@ -5,6 +5,8 @@
 // attention. A chunk's kept set is its clamped frame window plus the globals (section 一), so groups are runs of
 // consecutive chunks whose clamped windows coincide. The article caches one plan per geometry, at most four
 // (section 三, _Plan); this cache does the same and evicts the least recently used unreferenced plan.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime_api.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -14,6 +16,7 @@
 #include <cmath>
 #include <list>
 #include <mutex>
+#include <utility>
 
 #include "wa_internal.h"
 
@@ -60,6 +63,56 @@ struct wa_plan {
 namespace wa {
 
 static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+unsigned long long current_context_id() {
+  // Driver entry points, looked up once (a thread-safe static initialisation).
+  struct Fns {
+    PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    PFN_cuCtxGetId_v12000 get_id = nullptr;
+  };
+  static const Fns fns = [] {
+    Fns f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    cudaGetLastError();
+    return f;
+  }();
+  if (!fns.get_current || !fns.get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (fns.get_current(&ctx) != CUDA_SUCCESS) return 0;
+  if (!ctx) {  // the runtime has not made its primary context current on this thread yet: let it
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (fns.get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  }
+  unsigned long long id = 0;
+  if (fns.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id + 1;  // never 0 for a valid context
+}
+
+int ensure_smem_attr(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, unsigned long long>> done;  // (kernel, context) pairs already set
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lk(mu);
+  if (ctx != 0)
+    for (auto& d : done)
+      if (d.first == func && d.second == ctx) return 0;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return (int)e;
+  if (ctx != 0) done.emplace_back(func, ctx);  // context unknown: set it again on every launch
+  return 0;
+}
 
 wa_status make_geometry(int T, int S, int K, int r, int G, const wa_layout_t* layout, Geometry* geo) {
   if (!layout || !geo) return WA_ERR_INVALID;

@@ -82,8 +82,10 @@ typedef struct wa_plan wa_plan_t;
  *   T, S, K >= 1; r >= 0 (r >= number of chunks is valid: dense attention); G >= 0 (0 runs no global leg).
  *   layout: see wa_layout_t; B, H >= 1; D in {64, 128}; T*S + G < 2^31.
  * The plan holds the window groups, the work list of the attention kernel (uploaded to the device once) and
- * the global leg's workspace. Plans live in a process-wide cache of up to 4 geometries keyed on (device,
- * geometry, layout); the least recently used unreferenced entry is evicted. Each successful call returns a
+ * the global leg's workspace. The article builds its plan once per geometry and caches it (section 三, the _Plan
+ * object with its window groups and gather indices, kept per geometry); here plans live in a process-wide cache
+ * of up to 4 geometries keyed on (device, geometry, layout); the least recently used unreferenced entry is
+ * evicted. Each successful call returns a
  * reference that the caller must drop with wa_plan_release().
  * Errors: WA_ERR_INVALID (null pointers, bad geometry), WA_ERR_UNSUPPORTED (D), WA_ERR_OOM, WA_ERR_CUDA.
  */
@@ -217,9 +219,12 @@ const char* wa_status_string(wa_status s);
  * library's device code is loaded, until the process exits. It calls no cudaMalloc, cudaFree or other
  * allocating routine.
  *   Arguments: as wa_plan_create (geometry, layout) plus q, k, v, out and stream as wa_forward. The work list is
- *   rebuilt on the host and copied from ordinary host memory into the array on every call.
- *   The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
- *   current; make that first call before any stream capture.
+ *   built on the host per (b, h) slice and passed by value, as kernel parameters, to a small kernel that writes the
+ *   whole list into the array on every call (one launch per 800 entries of the per-slice list); no host memory is
+ *   read by the device after the call returns.
+ *   The first call in a CUDA context (the device's primary context, or a new one after cudaDeviceReset) looks up
+ *   the array's device address (cudaGetSymbolAddress) with that context current; make that first call before any
+ *   stream capture.
  *   Every call shares the one array: calls that overlap on the GPU (different streams or threads) race on it;
  *   calls on one stream are ordered. The array keeps the previous call's contents; the call clears what must
  *   start at zero.

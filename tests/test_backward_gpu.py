@@ -3,8 +3,10 @@ the gradients dq, dk, dv of sum(out * dout).
 
 Bars (float64 oracle on the same bf16 inputs):
   * lse: |lse_gpu - lse_ref| <= 2e-3 for every row (fp32 running sums over at most ~1e5 terms);
-  * gradients: per (b, h) slice ||g_gpu - g_ref||_F / ||g_ref||_F <= 1e-2 and max |g_gpu - g_ref| <= 5e-2 *
-    max |g_ref| (dS and P enter the tensor-core products as bf16, one rounding more than the forward).
+  * gradients: per (b, h) slice ||g_gpu - g_ref||_F / ||g_ref||_F <= 5e-3 and max |g_gpu - g_ref| <= 2e-2 *
+    max |g_ref|: the forward's relative bar. dS and P enter the tensor-core products as bf16, one rounding more
+    than the forward; the measured worst cases are 3.9e-3 relative and 6.9e-3 of the slice maximum (the sharpened
+    global keys), about 2.4e-3 and 3-5e-3 elsewhere.
 """
 import numpy as np
 import pytest
@@ -45,8 +47,8 @@ def test_forward_lse_full(cuda, w):
 
 
 # --------------------------------------------------------------------------------------------------- gradients
-GRAD_REL = 1e-2
-GRAD_ABS = 5e-2  # times max |reference| of the slice
+GRAD_REL = 5e-3
+GRAD_ABS = 2e-2  # times max |reference| of the slice
 
 
 def gpu_backward(wa, w, q, k, v, dout):
@@ -92,6 +94,11 @@ GRAD_CASES = [
                      k_global_scale=4.0),
     # at least 1024 global rows: doubled split length (2 splits), partial last global tile
     configs.Workload("bwd_long_globals", B=1, H=2, D=128, T=40, S=64, K=1, r=0, G=1100, global_pos=0, seed=49),
+    # B*H*L not a multiple of 4 (1 and 3 mod 4; bwd_one_token_frames has 2 mod 4): the split partials of the global
+    # rows, written with 16-byte stores, sit behind the B*H*L fp32 row dots in one workspace and must still start on
+    # a 16-byte boundary
+    configs.Workload("bwd_rows_1_mod_4", B=1, H=1, D=128, T=4, S=41, K=2, r=1, G=5, global_pos=0, seed=54),
+    configs.Workload("bwd_rows_3_mod_4_d64", B=1, H=3, D=64, T=7, S=13, K=3, r=0, G=2, global_pos=1, seed=55),
 ]
 
 

@@ -18,7 +18,7 @@ ABS_TOL = 3e-2
 
 
 def static_forward(wa, w, q, k, v):
-    out = torch.empty_like(q)
+    out = torch.full_like(q, float("nan"))  # a work item left out would leave NaN rows behind
     lay = wa.make_layout(w.B, w.L, w.H, w.D, w.global_pos)
     s = torch.cuda.current_stream().cuda_stream
     st = wa.lib().wa_forward_static(w.T, w.S, w.K, w.r, w.G, ctypes.byref(lay), ctypes.c_void_p(q.data_ptr()),
@@ -71,12 +71,17 @@ def test_static_scratch_rejects_oversized_geometry(cuda):
     torch.cuda.synchronize()
 
 
+# 1,000 window groups of one query tile each plus 63 global split items: 1,063 work items per (b, h), so the
+# allocation-free call writes its work list with two expansion launches (800 per launch)
+MANY_GROUPS = configs.Workload("many_groups", B=1, H=2, D=64, T=1000, S=64, K=1, r=0, G=64, global_pos=0, seed=71)
+
+
 def test_dynamic_claiming_matches_static_striding(cuda):
     """A plan's forward lets each CTA claim its next work item from a counter (the last CTA of a launch rewinds it);
-    wa_forward_static hands the same items out by static striding. Same items and the same arithmetic per item:
-    the results agree bit for bit, over several launches in a row on one plan (a counter left unrewound would make
-    the next launch skip its items and leave the NaN in place)."""
-    for w in (configs.MEDIUM, configs.RAGGED):
+    wa_forward_static writes the same items into its scratch on the device and hands them out by static striding.
+    Same items and the same arithmetic per item: the results agree bit for bit, over several launches in a row on
+    one plan (a counter left unrewound would make the next launch skip its items and leave the NaN in place)."""
+    for w in (configs.MEDIUM, configs.RAGGED, MANY_GROUPS):
         plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
         try:
             for seed in (5, 6, 7):
