@@ -10,6 +10,8 @@ rows scaled x2. Useful work counts only kept (query, key) pairs: 4*D flops per p
 
 Under torchrun (N > 1) every rank runs its own replica of the layer on its own GPU (no data exchange; the path is
 replicated, not sharded) and rank 0 prints one JSON line with the whole-job throughput over the slowest rank.
+``--shard heads`` instead shards one layer by heads across the ranks (all-to-all exchanges in and out, strong
+scaling).
 ``--impl reference`` times the CPU oracle on the host cores instead (rank 0 only), on a bounded row sample.
 """
 import argparse
@@ -45,6 +47,9 @@ def parse():
                     help="time the backward pass (dq, dk, dv through wa_backward) instead of the forward")
     ap.add_argument("--sweep", action="store_true",
                     help="auxiliary: one JSON line per sweep point (kept TFLOP/s vs window density), 1 GPU")
+    ap.add_argument("--shard", default="replicas", choices=["replicas", "heads"],
+                    help="under torchrun: independent replicas (default), or one layer sharded by heads across the "
+                         "ranks (Ulysses-style all-to-all of q, k, v in and of out back; strong scaling)")
     return ap.parse_args()
 
 
@@ -384,6 +389,72 @@ def run_backward(args, w):
         "gpu_launches": (3 + (1 if w.G > 0 else 0)) * args.steps, "clocks": clocks}), flush=True)
 
 
+def run_head_sharded(args, w, rank, world, local):
+    """One layer sharded by heads across the ranks: each rank starts from its shard of the packed sequence (all
+    heads), q, k and v go to head shards by all-to-all, each rank computes its H/N heads over the whole sequence with
+    the library, and the output goes back by all-to-all. Every step includes the four exchanges. Total work is the
+    layer's, whatever N (strong scaling)."""
+    import torch
+    import torch.distributed as dist
+    import chunk_windowed_softmax_gb300 as wa
+    from chunk_windowed_softmax_gb300 import _build, inputs, sharded
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    if w.H % world:
+        raise SystemExit(f"{w.H} heads do not split over {world} ranks")
+    sizes = sharded.even_seq_sizes(w.L, world)
+    off = sum(sizes[:rank])
+    q, k, v = inputs.make_qkv(w, device=dev)  # the same seed on every rank: the shards of one layer
+    qs, ks, vs = (t[:, off:off + sizes[rank]].contiguous() for t in (q, k, v))
+    del q, k, v
+    hn = w.H // world
+    plan = wa.Plan(w.T, w.S, w.K, w.r, w.G, w.B, hn, w.D, w.global_pos)
+    info = plan.info()
+    flops = 4.0 * w.D * info["kept_pairs"] * w.B * w.H  # the whole layer
+    oh = torch.empty(w.B, w.L, hn, w.D, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        return sharded.sharded_forward(qs, ks, vs, w.T, w.S, w.K, w.r, w.G, w.global_pos, seq_sizes=sizes,
+                                       attend=lambda qh, kh, vh: plan.forward(qh, kh, vh, out=oh))
+    for _ in range(max(3, args.warmup)):
+        step()
+    st = plan.check_error()
+    if st != 0:
+        raise SystemExit(f"device error during warm-up: {wa.wa_status_string(st)}")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev, world)
+    st = plan.check_error()
+    plan.close()
+    if st != 0:
+        raise SystemExit(f"device error during the timed steps: {wa.wa_status_string(st)}")
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w, {"parallelism": f"heads/{world}: all-to-all of q, k, v to head shards "
+                                                         f"and of out back, every step",
+                                          "seq_shard_rows": sizes, "heads_per_rank": hn,
+                                          "l2": "no flush: the tensors of a step are far larger than the 129 MB L2"
+                                          if w.name == "h3" else "not flushed"}),
+            "gpu_launches": (2 if w.G > 0 else 1) * args.steps}), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.sweep:
@@ -398,6 +469,9 @@ def main():
     w = workload(args.workload)
     if args.impl == "reference":
         run_reference(args, w, rank)
+        return
+    if args.shard == "heads":
+        run_head_sharded(args, w, rank, world, local)
         return
 
     import torch

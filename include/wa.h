@@ -43,7 +43,11 @@ typedef enum {
   WA_ERR_DEVICE_BOUNDS = 6    /* a device-side index check failed; the access was skipped */
 } wa_status;
 
-/* How the four tensors are laid out. All four (q, k, v, out) share it. */
+/* How the four tensors are laid out. All four (q, k, v, out) share it.
+ * A range of heads [h0, h0 + nh) of larger tensors is itself such a layout: H = nh with the larger tensors' strides,
+ * and every pointer advanced by h0 * stride_h elements. A head-sharded (Ulysses-style) run uses this, or the
+ * contiguous [B, L, H/N, D] head shard it receives from its all-to-all (MiniMax-H3 Ulysses pull request, sglang
+ * #43164, Motivation): (b, h) slices are independent, so a head range needs nothing from the other heads. */
 typedef struct {
   int32_t global_pos; /* 0 = globals after the frame tokens, 1 = before them */
   int32_t B;          /* batch */
