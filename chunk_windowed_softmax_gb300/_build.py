@@ -9,6 +9,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwa.so")
+# The index-checking debug library (-DWA_DEBUG: every work item is bounds-checked on the device before use); built
+# only on request (build(debug=True)), never by the default build.
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libwa_debug.so")
 SOURCES = ["wa_plan.cpp", "wa_kernels.cu", "wa_backward.cu", "wa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -20,10 +24,12 @@ def nvcc():
     return "nvcc"
 
 
-def _compile(src, verbose=False):
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src, verbose=False, debug=False):
+    obj = os.path.join(BUILD_DEBUG if debug else BUILD, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-c",
            os.path.join(CSRC, src), "-o", obj]
+    if debug:
+        cmd.insert(1, "-DWA_DEBUG")
     if verbose and src.endswith(".cu"):
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -32,26 +38,28 @@ def _compile(src, verbose=False):
     return obj, r.stderr
 
 
-def build(verbose=False, force=False):
-    """Compile the sources in parallel and link ``libwa.so``. Skips the work when the library is newer than
-    every source and header."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose=False, force=False, debug=False):
+    """Compile the sources in parallel and link ``libwa.so`` (``libwa_debug.so`` with ``debug``: the same sources
+    with the device-side index checks compiled in). Skips the work when the library is newer than every source and
+    header."""
+    lib = LIB_DEBUG if debug else LIB
+    os.makedirs(BUILD_DEBUG if debug else BUILD, exist_ok=True)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     deps.append(os.path.join(os.path.dirname(PKG), "include", "wa.h"))
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) > max(os.path.getmtime(d) for d in deps):
-        return LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) > max(os.path.getmtime(d) for d in deps):
+        return lib
     with ThreadPoolExecutor(len(SOURCES)) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
+        results = list(ex.map(lambda s: _compile(s, verbose, debug), SOURCES))
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -49,6 +49,7 @@ struct BwdParams {
   float scale;        // 1 / sqrt(D)
   int debug_flags;
   int* item_counter;  // ItemFeed counter (two ints, zero at launch); nullptr: static striding
+  int bh_count;       // B * H (index checks of a debug build)
 };
 
 // First row of the j-th 128-row tile of an item's segments, and how many of its rows belong to the segment.
@@ -278,6 +279,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = feed.claim_warp(n, abort_flag, err, ok);
         if (idx < 0) break;
         const Item it = load_item(prm.items, idx);
+#ifdef WA_DEBUG
+        if (!item_in_bounds(it, ItemBounds{prm.bh_count, prm.L, prm.g0, prm.G, prm.n_splits})) {
+          if (leader) {
+            atomicOr(err, kErrBounds);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+#endif
         const int b = it.bh / prm.H, h = it.bh % prm.H;
         const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
         const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
@@ -624,6 +635,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int idx = feed.claim_warp(n, abort_flag, err, ok);
       if (idx < 0) break;
       const Item it = load_item(prm.items, idx);
+#ifdef WA_DEBUG
+      if (!item_in_bounds(it, ItemBounds{prm.bh_count, prm.L, prm.g0, prm.G, prm.n_splits})) {
+        if (lane == 0) {
+          atomicOr(err, kErrBounds);
+          *abort_flag = 1;
+        }
+        ok = false;
+        break;
+      }
+#endif
       const int b = it.bh / prm.H, h = it.bh % prm.H;
       const int ntk = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
       const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
@@ -1057,6 +1078,7 @@ int launch_backward_d(const BackwardArgs& a, cudaStream_t s, int num_sms, void* 
   p.scale = (float)(1.0 / sqrt((double)D));
   p.debug_flags = a.debug_flags;
   p.item_counter = a.item_counter;
+  p.bh_count = l.B * l.H;
   const int grid = a.n_items < num_sms ? a.n_items : num_sms;
   if (grid > 0) {
     wa_dq_kernel<D><<<grid, kBwdThreads, DqCfg<D>::kSmemBytes, s>>>(mq, mk, mv, mdo, p);

@@ -30,6 +30,25 @@ __device__ __forceinline__ int tile_valid(const Item& it, int j, int nt0) {
                  : min(kTileRows, it.s1_hi - (it.s1_lo + (j - nt0) * kTileRows));
 }
 
+// Index checks of a debug build (compiled with -DWA_DEBUG; they stand in for a memory checker). An item is in
+// bounds when its head index is below B*H, its query rows are a non-empty range of at most two tiles inside [0, L),
+// segment 0 is a non-empty and segment 1 a possibly empty range inside [0, L), and a global split item's split index
+// is below n_splits and its query rows lie inside the global rows [g0, g0 + G). Every copy coordinate and store row
+// of the kernels derives from these fields. The claiming thread checks each item before any role uses it; a failed
+// check latches the bounds error and unwinds the CTA without touching memory for that item.
+struct ItemBounds {
+  int bh_count, L, g0, G, n_splits;
+};
+__device__ __forceinline__ bool item_in_bounds(const Item& it, const ItemBounds& b) {
+  const bool head = it.bh >= 0 && it.bh < b.bh_count;
+  const bool rows = it.q_lo >= 0 && it.q_lo < it.q_hi && it.q_hi <= b.L && it.q_hi - it.q_lo <= kItemRows;
+  const bool seg0 = it.s0_lo >= 0 && it.s0_lo < it.s0_hi && it.s0_hi <= b.L;
+  const bool seg1 = it.s1_lo >= 0 && it.s1_lo <= it.s1_hi && it.s1_hi <= b.L;
+  const bool split = it.split == -1 ||
+                     (it.split >= 0 && it.split < b.n_splits && it.q_lo >= b.g0 && it.q_hi <= b.g0 + b.G);
+  return head && rows && seg0 && seg1 && split;
+}
+
 // Zero rows [valid, 128) of a 128-row tile held in shared memory as `boxes` consecutive boxes of 128 rows x 128
 // bytes (a row of a box is 128 contiguous bytes, so the 128-byte swizzle inside a row does not matter). A segment's
 // last tile is copied whole and so holds rows past the segment's end: tokens outside the rows' kept sets, or past

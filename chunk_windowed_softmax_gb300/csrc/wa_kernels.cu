@@ -114,6 +114,7 @@ struct Params {
   float* lse;     // optional [B][H][L] row log-sum-exp output (natural log); nullptr when not wanted
   int L;
   int* item_counter;  // ItemFeed counter (two ints, zero at launch); nullptr: static striding
+  int bh_count;       // B * H (index checks of a debug build)
 };
 
 // Shared-memory barrier layout, relative to the barrier block: q_full[2] q_empty[2] s_full[2] p_full[2]
@@ -251,7 +252,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t n = 0; ok; ++n) {
         const int idx = feed.claim_warp(n, abort_flag, err, ok);
         if (idx < 0) break;
+#ifdef WA_DEBUG
+        Item it = load_item(prm.items, idx);
+        if ((prm.debug_flags & 8) && n == 0 && blockIdx.x == 0)
+          it.s0_hi = prm.L + 1000;  // test hook: a key segment past the sequence (the check must catch it)
+        if (!item_in_bounds(it, ItemBounds{prm.bh_count, prm.L, prm.g0, prm.G, prm.n_splits})) {
+          if (leader) {
+            atomicOr(err, kErrBounds);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+#else
         const Item it = load_item(prm.items, idx);
+#endif
         const int b = it.bh / prm.H, h = it.bh % prm.H;
         const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
 #pragma unroll
@@ -694,6 +709,7 @@ int launch_attention_d(const LaunchArgs& a, cudaStream_t s, int num_sms) {
   p.lse = a.lse;
   p.L = (int)a.geo->L;
   p.item_counter = a.item_counter;
+  p.bh_count = l.B * l.H;
   const int grid = a.n_items < num_sms ? a.n_items : num_sms;
   window_attention_kernel<D, kF8><<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mo, p);
   return (int)cudaGetLastError();

@@ -246,7 +246,10 @@ wa_status wa_forward_static(int T, int S, int K, int r, int G, const wa_layout_t
  * consumer's bounded wait runs out (about 2 s), the kernel unwinds and latches WA_ERR_DEVICE_TIMEOUT, which
  * wa_plan_check_error() then reports. flags & 2 and flags & 4 do the same to the backward's dq kernel and dk/dv
  * kernel (one query-tile copy is never issued). The device stays usable; later calls with flags == 0 are
- * correct. Returns WA_ERR_INVALID for a NULL plan.
+ * correct. flags & 8 (only in the index-checking debug build, libwa_debug.so, compiled with -DWA_DEBUG): the first
+ * work item of the forward's first CTA is given a key segment past the end of the sequence; the device-side check
+ * rejects it before any copy, the CTA unwinds and WA_ERR_DEVICE_BOUNDS is latched. Returns WA_ERR_INVALID for a
+ * NULL plan.
  */
 int wa_plan_set_debug_flags(wa_plan_t* plan, int flags);
 
