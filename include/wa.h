@@ -168,8 +168,9 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
  * Errors (synchronous, nothing launched): WA_ERR_INVALID for null or misaligned pointers, or when dq, dk or dv
  * overlaps each other or any input; WA_ERR_OOM when the workspace cannot be allocated; WA_ERR_CUDA when a launch
  * fails. Device-side failures: see wa_plan_check_error(); besides the wait watchdog, the dk/dv kernel at D = 128
- * reports WA_ERR_DEVICE_BOUNDS (and computes nothing) if the device gives it a dynamic shared-memory window that is
- * not 1024-byte aligned, since its buffers leave no room to realign it.
+ * reports WA_ERR_DEVICE_BOUNDS (and computes nothing) if the device gives it a dynamic shared-memory window more
+ * than 768 bytes short of a 1024-byte boundary, since its buffers leave only that much room to realign it (any
+ * window on a 256-byte boundary is fine).
  */
 wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void* v, const void* out, const void* dout,
                       const float* lse, void* dq, void* dk, void* dv, wa_stream_t stream);
