@@ -90,3 +90,24 @@ def test_fp8_rejects_bad_scales_and_head_dim(cuda):
         assert lib.wa_forward_fp8(*args, 1.0, float("nan"), None) == 1
     finally:
         plan.close()
+
+
+def random_fp8_geometries(n, seed):
+    """Seeded random geometries for the e4m3 path (D = 128): ragged chunks, both global placements, r past nc."""
+    import random
+    rnd = random.Random(seed)
+    out = []
+    for i in range(n):
+        T = rnd.randint(1, 14)
+        K = rnd.randint(1, 5)
+        nc = -(-T // K)
+        out.append(configs.Workload(f"fp8_rand{i}", B=rnd.randint(1, 2), H=rnd.randint(1, 3), D=128, T=T,
+                                    S=rnd.randint(1, 97), K=K, r=rnd.randint(0, nc + 1),
+                                    G=rnd.choice([0, 1, rnd.randint(2, 300)]), global_pos=rnd.randint(0, 1),
+                                    seed=4000 + i))
+    return out
+
+
+@pytest.mark.parametrize("w", random_fp8_geometries(10, seed=9), ids=lambda w: w.name)
+def test_fp8_random_geometries(cuda, w):
+    run(cuda, w)

@@ -78,6 +78,42 @@ def test_sequence_head_exchange_and_sharded_layer_gloo():
     assert all(p.exitcode == 0 for p in procs)
 
 
+def _worker3(rank, world, port, q):
+    """Three ranks, six heads, sequence shards of unequal sizes (one of them empty): round trip."""
+    try:
+        sys.path.insert(0, ROOT)
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        from chunk_windowed_softmax_gb300 import sharded
+        g = torch.Generator().manual_seed(9)
+        full = torch.randn(2, 41, 6, 4, generator=g).to(torch.bfloat16)
+        for sizes in (sharded.even_seq_sizes(41, world), [1, 30, 10], [20, 0, 21]):
+            off = sum(sizes[:rank])
+            x = full[:, off:off + sizes[rank]].contiguous()
+            xh = sharded.seq_to_heads(x, sizes)
+            assert torch.equal(xh, full[:, :, 2 * rank:2 * rank + 2]), "head shard"
+            assert torch.equal(sharded.heads_to_seq(xh, sizes), x), "round trip"
+        q.put((rank, "ok"))
+        dist.barrier()
+        dist.destroy_process_group()
+    except Exception as e:
+        q.put((rank, repr(e)))
+
+
+def test_exchange_three_ranks_uneven_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_worker3, args=(r, 3, port, q)) for r in range(3)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert res == {0: "ok", 1: "ok", 2: "ok"}, res
+    assert all(p.exitcode == 0 for p in procs)
+
+
 def test_even_seq_sizes():
     from chunk_windowed_softmax_gb300 import sharded
     assert sharded.even_seq_sizes(99968, 8) == [12496] * 8

@@ -74,6 +74,8 @@ def test_static_scratch_rejects_oversized_geometry(cuda):
 # 1,000 window groups of one query tile each plus 63 global split items: 1,063 work items per (b, h), so the
 # allocation-free call writes its work list with two expansion launches (800 per launch)
 MANY_GROUPS = configs.Workload("many_groups", B=1, H=2, D=64, T=1000, S=64, K=1, r=0, G=64, global_pos=0, seed=71)
+# head dim 64 with the globals before the frames
+D64_FRONT = configs.Workload("d64_front", B=2, H=3, D=64, T=13, S=37, K=4, r=2, G=130, global_pos=1, seed=72)
 
 
 def test_dynamic_claiming_matches_static_striding(cuda):
@@ -81,7 +83,7 @@ def test_dynamic_claiming_matches_static_striding(cuda):
     wa_forward_static writes the same items into its scratch on the device and hands them out by static striding.
     Same items and the same arithmetic per item: the results agree bit for bit, over several launches in a row on
     one plan (a counter left unrewound would make the next launch skip its items and leave the NaN in place)."""
-    for w in (configs.MEDIUM, configs.RAGGED, MANY_GROUPS):
+    for w in (configs.MEDIUM, configs.RAGGED, MANY_GROUPS, D64_FRONT):
         plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
         try:
             for seed in (5, 6, 7):
