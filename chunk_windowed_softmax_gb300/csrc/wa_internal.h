@@ -3,6 +3,8 @@
 
 #include <stdint.h>
 
+#include <new>
+#include <stdexcept>
 #include <utility>
 #include <vector>
 
@@ -61,6 +63,20 @@ wa_status make_geometry(int T, int S, int K, int r, int G, const wa_layout_t* la
 void build_host_plan(const Geometry& geo, HostPlan* hp);
 // Build the host-buffer forward's piece schedule for a plan (host only).
 void build_host_schedule(const HostPlan& hp, HostSchedule* hs);
+// Run `build` (which fills host-side tables) so that no C++ exception leaves the C ABI: a failed host allocation
+// becomes WA_ERR_OOM. Geometries that pass make_geometry have bounded tables, so this is only reached when the host
+// itself is out of memory.
+template <class F>
+wa_status host_tables(F&& build) {
+  try {
+    build();
+  } catch (const std::bad_alloc&) {
+    return WA_ERR_OOM;
+  } catch (const std::length_error&) {
+    return WA_ERR_OOM;
+  }
+  return WA_OK;
+}
 
 // Arguments of one attention launch (device pointers; tensor maps are built by the launcher).
 struct LaunchArgs {

@@ -86,7 +86,7 @@ extern "C" wa_status wa_forward_static(int T, int S, int K, int r, int G, const 
   g1.layout.B = 1;
   g1.layout.H = 1;
   wa::HostPlan hp;
-  wa::build_host_plan(g1, &hp);
+  if (wa::host_tables([&] { wa::build_host_plan(g1, &hp); }) != WA_OK) return WA_ERR_OOM;
   const int BH = l.B * l.H;
   const size_t n_tpl = hp.items.size();
   const size_t n_items = n_tpl * (size_t)BH;

@@ -13,7 +13,10 @@
 #include <string.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
+#include <new>
+#include <stdexcept>
 #include <list>
 #include <mutex>
 #include <utility>
@@ -133,8 +136,18 @@ wa_status make_geometry(int T, int S, int K, int r, int G, const wa_layout_t* la
   for (auto& a : ax) {
     if (a.extent == 1) continue;
     if (a.stride < span) return WA_ERR_INVALID;
+    // Element offsets stay far inside int64 (and byte offsets too): 2^60 elements is past any device's memory.
+    if (a.stride > (((int64_t)1 << 60) / a.extent)) return WA_ERR_UNSUPPORTED;
     span = a.stride * a.extent;
   }
+  // Work items carry 32-bit (b, h) indices and are counted in 32 bits: bound the count over all B*H slices. Per
+  // slice at most ceil(F / item rows) + nc window items (one partial item per group, at most nc groups) and, with
+  // globals, ceil(G / item rows) items for each of at most 64 key splits. Any geometry whose four tensors fit in
+  // device memory stays far below the bound (B*H*L < 2^30 elements of D >= 64 at 288 GB).
+  const int64_t BH = (int64_t)l.B * l.H;
+  const int64_t nc = cdiv(T, K);
+  const int64_t per_slice = cdiv((int64_t)T * S, kItemRows) + nc + (G > 0 ? 64 * cdiv(G, kItemRows) : 0);
+  if (per_slice > (int64_t)INT32_MAX / BH) return WA_ERR_UNSUPPORTED;
   geo->T = T; geo->S = S; geo->K = K; geo->r = r; geo->G = G;
   geo->layout = l;
   geo->nc = cdiv(T, K);
@@ -196,7 +209,7 @@ void build_host_plan(const Geometry& g, HostPlan* hp) {
   }
   hp->n_splits = n_splits;
 
-  const int BH = g.layout.B * g.layout.H;
+  const int BH = (int)((int64_t)g.layout.B * g.layout.H);  // below 2^31: bounded by make_geometry
   std::vector<Item> items;
   for (int bh = 0; bh < BH; ++bh) {
     for (auto& gr : hp->groups) {
@@ -437,9 +450,13 @@ cudaError_t dev_alloc(T** ptr, size_t bytes) {
 }
 
 wa_status create_uncached(const wa::Geometry& g, int dev, wa_plan** out) {
-  wa_plan* p = new wa_plan();
+  wa_plan* p = new (std::nothrow) wa_plan();
+  if (!p) return WA_ERR_OOM;
   p->device = dev;
-  wa::build_host_plan(g, &p->hp);
+  if (wa::host_tables([&] { wa::build_host_plan(g, &p->hp); }) != WA_OK) {
+    delete p;
+    return WA_ERR_OOM;
+  }
   if (cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     delete p;
     return WA_ERR_CUDA;
@@ -502,7 +519,8 @@ wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layou
   wa_status st = wa::make_geometry(T, S, K, r, G, layout, &g);
   if (st != WA_OK) return st;
   wa::HostPlan hp;
-  wa::build_host_plan(g, &hp);
+  st = wa::host_tables([&] { wa::build_host_plan(g, &hp); });
+  if (st != WA_OK) return st;
   *info = hp.info;
   if (groups)
     for (int64_t i = 0; i < std::min<int64_t>(groups_cap, (int64_t)hp.groups.size()); ++i) groups[i] = hp.groups[i];
@@ -524,9 +542,12 @@ wa_status wa_host_schedule_describe(int T, int S, int K, int r, int G, const wa_
   wa_status st = wa::make_geometry(T, S, K, r, G, layout, &g);
   if (st != WA_OK) return st;
   wa::HostPlan hp;
-  wa::build_host_plan(g, &hp);
   wa::HostSchedule hs;
-  wa::build_host_schedule(hp, &hs);
+  st = wa::host_tables([&] {
+    wa::build_host_plan(g, &hp);
+    wa::build_host_schedule(hp, &hs);
+  });
+  if (st != WA_OK) return st;
   *n_pieces = (int64_t)hs.pieces.size();
   *row_pieces = hs.rows ? 1 : 0;
   if (pieces)
@@ -856,7 +877,8 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
   cudaStream_t s = (cudaStream_t)stream;
   std::lock_guard<std::mutex> lk(plan->mu);
   const size_t stage_span = (span + 255) / 256 * 256;
-  wa_status st = prepare_host_path(plan, stage_span);
+  wa_status st = WA_OK;
+  if (wa::host_tables([&] { st = prepare_host_path(plan, stage_span); }) != WA_OK) return WA_ERR_OOM;
   if (st != WA_OK) return st;
   if (plan->have_last && plan->last_stream != s) {
     if (cudaStreamWaitEvent(s, plan->done, 0) != cudaSuccess) return WA_ERR_CUDA;

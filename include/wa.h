@@ -36,8 +36,8 @@ typedef struct CUstream_st* wa_stream_t;
 typedef enum {
   WA_OK = 0,
   WA_ERR_INVALID = 1,         /* bad argument: geometry, pointer, alignment, stride, aliasing */
-  WA_ERR_UNSUPPORTED = 2,     /* valid but not built: head dim other than 64/128, sizes past int32 rows */
-  WA_ERR_OOM = 3,             /* device allocation of the plan's tables or workspace failed */
+  WA_ERR_UNSUPPORTED = 2,     /* valid but not built: head dim other than 64/128, sizes past int32 rows or items */
+  WA_ERR_OOM = 3,             /* device (or host) allocation of the plan's tables or workspace failed */
   WA_ERR_CUDA = 4,            /* a CUDA call failed (launch error, no device, wrong architecture) */
   WA_ERR_DEVICE_TIMEOUT = 5,  /* a device-side wait ran past its limit; the kernel gave up and returned */
   WA_ERR_DEVICE_BOUNDS = 6    /* a device-side index check failed; the access was skipped */
@@ -84,14 +84,17 @@ typedef struct wa_plan wa_plan_t;
 /*
  * Build (or fetch from the cache) the plan for one geometry on the current CUDA device.
  *   T, S, K >= 1; r >= 0 (r >= number of chunks is valid: dense attention); G >= 0 (0 runs no global leg).
- *   layout: see wa_layout_t; B, H >= 1; D in {64, 128}; T*S + G < 2^31.
+ *   layout: see wa_layout_t; B, H >= 1; D in {64, 128}; T*S + G < 2^31. Work items carry 32-bit indices, so
+ *   B*H * (ceil(T*S / 256) + ceil(T / K) + 64 * ceil(G / 256)) must stay below 2^31, and no stride times its
+ *   extent may reach 2^60 elements; any geometry whose tensors fit in device memory is far inside both bounds.
  * The plan holds the window groups, the work list of the attention kernel (uploaded to the device once) and
  * the global leg's workspace. The article builds its plan once per geometry and caches it (section 三, the _Plan
  * object with its window groups and gather indices, kept per geometry); here plans live in a process-wide cache
  * of up to 4 geometries keyed on (device, geometry, layout); the least recently used unreferenced entry is
  * evicted. Each successful call returns a
  * reference that the caller must drop with wa_plan_release().
- * Errors: WA_ERR_INVALID (null pointers, bad geometry), WA_ERR_UNSUPPORTED (D), WA_ERR_OOM, WA_ERR_CUDA.
+ * Errors: WA_ERR_INVALID (null pointers, bad geometry), WA_ERR_UNSUPPORTED (D, the bounds above), WA_ERR_OOM (a
+ * device or host allocation failed; no C++ exception leaves the library), WA_ERR_CUDA.
  */
 wa_status wa_plan_create(int T, int S, int K, int r, int G, const wa_layout_t* layout, wa_plan_t** out);
 

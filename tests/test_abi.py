@@ -80,3 +80,47 @@ def test_describe_without_device(walib):
     assert info["n_groups"] == 3 and len(groups) == 3
     assert info["kept_pairs"] == 8768
     assert len(items) == info["n_items"]
+
+
+# Sizes past what 32-bit work-item fields can index, and strides whose offsets would leave int64: rejected as
+# WA_ERR_UNSUPPORTED by every entry point that takes a geometry, before any table is built or device touched.
+HUGE = [
+    dict(T=4, S=8, K=2, r=1, G=3, B=65536, H=65536),         # B*H = 2^32 slices
+    dict(T=1000, S=1000, K=4, r=1, G=0, B=1, H=1 << 20),      # 4,907 items per slice x 2^20 slices
+    dict(T=8, S=1, K=1, r=0, G=1 << 20, B=1, H=16384),        # bound: (1 + 8 + 64 x 4,096) x 2^14 slices
+]
+
+
+@pytest.mark.parametrize("a", HUGE)
+def test_item_count_past_int32_is_unsupported(walib, a):
+    L = a["T"] * a["S"] + a["G"]
+    lay = walib.make_layout(a["B"], L, a["H"], 64, 0)
+    lib = walib.lib()
+    info = walib.wa_plan_info_t()
+    assert lib.wa_geometry_describe(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), ctypes.byref(info),
+                                    None, 0, None, 0) == 2
+    h = ctypes.c_void_p()
+    assert lib.wa_plan_create(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), ctypes.byref(h)) == 2
+    assert not h.value
+    n = ctypes.c_int64()
+    assert lib.wa_host_schedule_describe(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), None, 0, None, 0,
+                                         None, 0, ctypes.byref(n), ctypes.byref(n), ctypes.byref(ctypes.c_int32())) == 2
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: the geometry is rejected first
+    assert lib.wa_forward_static(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), p, p, p,
+                                 ctypes.c_void_p(1 << 21), None) == 2
+
+
+def test_stride_offsets_past_int64_are_unsupported(walib):
+    lay = walib.make_layout(4, 35, 1, 64, 0, strides=(1 << 61, 64, 64))
+    info = walib.wa_plan_info_t()
+    assert walib.lib().wa_geometry_describe(4, 8, 2, 1, 3, ctypes.byref(lay), ctypes.byref(info), None, 0, None,
+                                            0) == 2
+
+
+def test_largest_item_count_just_inside_int32_is_described(walib):
+    # Item count per slice bounded by 2 + 1 = 3 (one window item, one group, no globals): the bound allows
+    # floor((2^31 - 1) / 3) slices; a smaller but still large B*H is described without building any device state.
+    H = 1 << 16
+    lay = walib.make_layout(1, 16, H, 64, 0)
+    info, groups, _ = walib.wa_geometry_describe(2, 8, 2, 0, 0, lay)
+    assert info["n_items"] == H and len(groups) == 1
