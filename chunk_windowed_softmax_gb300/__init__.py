@@ -367,3 +367,51 @@ def forward(q, k, v, T, S, K, r, G, global_pos=0, out=None):
         return plan.forward(q, k, v, out=out)
     finally:
         plan.close()
+
+
+_autograd_fn = None
+
+
+def _window_softmax_fn():
+    """The torch.autograd.Function behind window_softmax_decomposed (defined on first use: torch is imported lazily
+    by this module)."""
+    global _autograd_fn
+    if _autograd_fn is None:
+        import torch
+
+        class WindowSoftmaxDecomposed(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, plan):
+                out, lse = plan.forward_lse(q, k, v)
+                ctx.plan = plan
+                ctx.save_for_backward(q, k, v, out, lse)
+                return out
+
+            @staticmethod
+            def backward(ctx, dout):
+                q, k, v, out, lse = ctx.saved_tensors
+                lay = ctx.plan.layout
+                strides = (lay.stride_b, lay.stride_l, lay.stride_h, 1)
+                if dout.dtype != torch.bfloat16 or tuple(dout.stride()) != strides:
+                    # the incoming gradient in the plan's layout (e.g. an expanded gradient of a sum has stride 0)
+                    dout = torch.empty_strided(dout.shape, strides, dtype=torch.bfloat16,
+                                               device=dout.device).copy_(dout)
+                dq, dk, dv = ctx.plan.backward(q, k, v, out, dout, lse)
+                need = ctx.needs_input_grad
+                return (dq if need[0] else None, dk if need[1] else None, dv if need[2] else None, None)
+
+        _autograd_fn = WindowSoftmaxDecomposed
+    return _autograd_fn
+
+
+def window_softmax_decomposed(q, k, v, T, S, K, r, G, global_pos=0):
+    """Differentiable window attention of bf16 CUDA tensors q, k, v ([B, L, H, D], any stride order with D
+    contiguous): the forward keeps each row's log-sum-exp, and autograd's backward runs this library's gradient
+    kernels (dq, dk, dv) from it. This is the decomposed path of the VDN-Minimax-H3 window-attention article
+    (section 三, window_softmax_decomposed) made usable for training, which the article otherwise leaves to its
+    differentiable mask-based path (section 五). Every output row depends only on its kept set (section 一)."""
+    B, L, H, D = q.shape
+    if L != T * S + G:
+        raise ValueError(f"q has {L} rows; the geometry needs T*S + G = {T * S + G}")
+    plan = Plan(T, S, K, r, G, B, H, D, global_pos, strides=tuple(q.stride()[:3]))
+    return _window_softmax_fn().apply(q, k, v, plan)
