@@ -27,7 +27,9 @@
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [384, 384+D). P_t (bf16) overwrites the
 // first 64 columns of S_t and is the A operand of the P.V MMA, read straight from TMEM.
 // The two query tiles ping-pong: while one warpgroup runs the softmax of its tile, the tensor core works on the
-// other tile's products.
+// other tile's products. An item with a single query tile (the rows of a group past its last full pair of tiles)
+// alternates its key tiles between the two slots instead and merges the two halves at the end, so that it keeps
+// the ping-pong too.
 //
 // Softmax state is fp32 in registers: a reference max m (in log2 units of the scaled score) and row sum l. Each
 // step exponentiates against m and checks only the step's row sum: the exact row max is taken (and m raised, O
@@ -90,9 +92,12 @@ struct Cfg {
   static constexpr int kBarOff = kStageOff + (kStage ? 2 * kStageTileBytes : 0);
   // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] drain b_full[kLag] b_empty[kLag]
   //           item ring full[kItemRingSlots] empty[kItemRingSlots]  stage_full[2] stage_free[2] v_land
-  static constexpr int kNumBars = 11 + 2 * kLag + 2 * kItemRingSlots + 5;
+  //           xchg_full o1_free
+  static constexpr int kNumBars = 11 + 2 * kLag + 2 * kItemRingSlots + 7;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM address, abort flag, 2 spare words, item ring
-  static constexpr int kSmemBytes = kMiscOff + 16 + 4 * kItemRingSlots + 1024;  // + slack for 1024-byte alignment
+  // (m, l) of the 128 rows of an alternating-key item's second half, handed to the first warpgroup (8 bytes a row)
+  static constexpr int kXchgOff = kMiscOff + 16 + 4 * kItemRingSlots;
+  static constexpr int kSmemBytes = kXchgOff + kTileRows * 8 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t kTmemO = 256;
   static constexpr uint32_t kIdescS = kF8 ? idesc_e4m3_f32(128, 128)
                                          : idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
@@ -141,7 +146,17 @@ struct BarAddr {
   }
   // a segment's last V tile lands here (not on its bundle's barrier) so the producer can clean it first
   __device__ __forceinline__ uint32_t v_land() const { return base + 8 * (15 + 2 * NB + 2 * kItemRingSlots); }
+  // alternating-key items: the second warpgroup's (m, l) are in shared memory (xchg_full); the first warpgroup has
+  // read them and the second half's O out of TMEM (o1_free)
+  __device__ __forceinline__ uint32_t xchg_full() const { return base + 8 * (16 + 2 * NB + 2 * kItemRingSlots); }
+  __device__ __forceinline__ uint32_t o1_free() const { return base + 8 * (17 + 2 * NB + 2 * kItemRingSlots); }
 };
+
+// An item with a single query tile and at least two key tiles runs with alternating keys: key tile j goes to tile
+// slot j % 2, so the two slots (their S/P and O regions in TMEM and their softmax warpgroups) ping-pong on the same
+// query rows exactly as two query tiles would, and the tile costs half the time it would alone. Each slot keeps its
+// own (O, m, l) over its keys; the first warpgroup merges the two by log-sum-exp in the epilogue.
+__device__ __forceinline__ bool alternating_keys(int ntq, int nt) { return ntq == 1 && nt >= 2; }
 
 // Exponentiate one 128-column score row into bf16 P (written to TMEM over the row's S columns, 16 columns per
 // store) and return the fp32 row sum.
@@ -208,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.stage_free(t), 1);  // the store issuer, once the copy engine has read the stage
     }
     mbar_init(bars.v_land(), 1);
+    mbar_init(bars.xchg_full(), 4);  // one arrive per warp of the second warpgroup
+    mbar_init(bars.o1_free(), 4);    // one arrive per warp of the first warpgroup
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -367,18 +384,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tmem + C::kTmemO + t * 128, tmem + t * 128 + kk * 8, d0 + ((kk * 2048) >> 4), desc_hi,
                  C::kIdescPV, (acc_first || kk > 0) ? 1u : 0u);
       };
-      // S_t = Q_t K^T, both K-major; each MMA takes 32 bytes of K (16 bf16 or 32 e4m3 elements) inside a
-      // 128-byte swizzle row, then moves to the next box
-      auto issue_s = [&](int t, uint32_t kslot) {
-        const uint32_t q0 = (uint32_t)dq + ((t * C::kQTileBytes) >> 4);
+      // S_u = Q_qt K^T into the S region of slot u, both K-major; each MMA takes 32 bytes of K (16 bf16 or 32
+      // e4m3 elements) inside a 128-byte swizzle row, then moves to the next box
+      auto issue_s = [&](int qt, int u, uint32_t kslot) {
+        const uint32_t q0 = (uint32_t)dq + ((qt * C::kQTileBytes) >> 4);
         const uint32_t k0 = (uint32_t)dk + ((kslot * C::kQTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::kSKSteps; ++kk) {
           const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
           if constexpr (kF8)
-            mma_ss_f8(tmem + t * 128, q0 + off, k0 + off, desc_hi, C::kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss_f8(tmem + u * 128, q0 + off, k0 + off, desc_hi, C::kIdescS, kk > 0 ? 1u : 0u);
           else
-            mma_ss(tmem + t * 128, q0 + off, k0 + off, desc_hi, C::kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + u * 128, q0 + off, k0 + off, desc_hi, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       for (uint32_t n = 0; ok; ++n) {
@@ -395,6 +412,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_n1++;
         }
         if (!ok) break;
+        if (alternating_keys(ntq, nt)) {
+          // Step j: S = Q_0 K_j^T into slot j % 2 first (that region was last read by the P.V of key tile j - 2,
+          // issued one step earlier: the tensor pipe runs in issue order), then O_u += P_u(j-1) V_{j-1} for the
+          // slot u of key tile j - 1 once its softmax has written P; j = nt only drains. Each slot's O is complete
+          // after its last key tile (nt - 1 or nt - 2).
+          for (int j = 0; j <= nt; ++j) {
+            ok = mbar_wait_warp(bars.b_full(b_n), (b_n / C::kLag) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t kslot = k_n % C::kKSlots, vslot = v_n % C::kVSlots;
+            if (j < nt) {
+              issue_s(0, j & 1, kslot);
+              mma_commit(bars.s_full(j & 1));
+            }
+            if (j > 0) {
+              const int u = (j - 1) & 1;
+              uint32_t& pn = u ? p_n1 : p_n0;
+              ok = mbar_wait_warp(bars.p_full(u), pn & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+              pn++;
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(u, vslot, j - 1 >= 2);
+              if (j - 1 >= nt - 2) mma_commit(bars.o_full(u));
+            }
+            mma_commit(bars.b_empty(b_n));
+            if (j == nt - 1) mma_commit(bars.q_empty(0));
+            if (j < nt) k_n++;
+            if (j >= 1) v_n++;
+            b_n++;
+          }
+          continue;
+        }
         // Step j: O_t += P_t(j-1) V_{j-1} (j >= 1), then S_t = Q_t K_j^T (j < nt), per tile; j = nt only drains.
         for (int j = 0; j <= nt; ++j) {
           ok = mbar_wait_warp(bars.b_full(b_n), (b_n / C::kLag) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
@@ -414,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j == nt) mma_commit(bars.o_full(t));
             }
             if (j < nt) {
-              issue_s(t, kslot);  // S_t = Q_t K_j^T
+              issue_s(t, t, kslot);  // S_t = Q_t K_j^T
               mma_commit(bars.s_full(t));
             }
           }
@@ -445,80 +494,144 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + C::kTmemO + t * 128;
     const uint32_t bar_s = bars.s_full(t), bar_p = bars.p_full(t), bar_o = bars.o_full(t);
     uint32_t s_n = 0, o_n = 0, st_n = 0;  // st_n: staged halves of this warpgroup
+    // Alternating-key items (one query tile, keys alternating between the slots): xk_n counts them (the phase of
+    // xchg_full and o1_free); the first warpgroup counts the completions of slot 1's o_full in o1_n (it waits on
+    // that barrier only in these items); the second warpgroup must see o1_free before its next item (whose P.V
+    // overwrites O_1, which the first warpgroup reads in the merge, and which may write the exchange again).
+    uint32_t xk_n = 0, o1_n = 0;
+    bool o1_pending = false;
+    const uint32_t xchg = s_base + C::kXchgOff + row_in_tile * 8;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
       const int idx = feed.fetch(n, abort_flag, err, ok);  // every softmax warp takes every item
       if (idx < 0) break;
       const Item it = load_item(prm.items, idx);
       const int ntq = (it.q_hi - it.q_lo > kTileRows) ? 2 : 1;
-      if (t >= ntq) continue;
       const int nt0 = seg_tiles(it.s0_lo, it.s0_hi);
       const int nt = nt0 + seg_tiles(it.s1_lo, it.s1_hi);
-      float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nt; ++j) {
-        const int valid = tile_valid(it, j, nt0);
-        ok = mbar_wait(bar_s, s_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+      const bool alt = alternating_keys(ntq, nt);
+      if (t == 0 && ntq > 1) o1_n++;  // slot 1's O completes once in every two-tile item
+      if (t >= ntq && !alt) continue;
+      if (o1_pending) {  // this item's first P would let a P.V overwrite O_1: wait until the merge has read it
+        ok = mbar_wait(bars.o1_free(), (xk_n - 1) & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
-        s_n++;
+        o1_pending = false;
         if (!ok) break;
-        tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld_x128(tS, sr);
-        float(&s)[128] = *reinterpret_cast<float(*)[128]>(sr);
-        if (valid < kTileRows) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= valid) s[c] = -INFINITY;
-        }
-        // P = 2^(s*c - m) against the current reference m, and its row sum. The reference only has to keep P finite
-        // and within a sane range, not equal the row max: the final normalisation divides by l built against the
-        // same reference. So the exact row max is computed only when this step's sum exceeds 2^16 (or is not
-        // finite; the first step of an item starts from m = -inf): then the warp takes the max, raises m, redoes
-        // the exponentials and rescales l and, after the first step, O.
-        float row_sum = exp_store_row(s, prm.c_scale, -m, tS);
-        const bool need = !(row_sum <= kLazyLimit);
-        if (__any_sync(0xffffffffu, need)) {  // warp-uniform: tcgen05.ld/st are warp-collective
-          float alpha = 1.f;
-          if (need) {
-            // Row max: 8 independent chains of three-input maxima over 16 columns each.
-            float mx[8];
-#pragma unroll
-            for (int a = 0; a < 8; ++a) {
-              mx[a] = fmaxf(s[16 * a], s[16 * a + 15]);
-#pragma unroll
-              for (int c = 1; c < 15; c += 2) mx[a] = max3(mx[a], s[16 * a + c], s[16 * a + c + 1]);
-            }
-            const float m_cand =
-                fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7])) * prm.c_scale;
-            alpha = j == 0 ? 0.f : ex2(m - m_cand);
-            m = m_cand;
-          }
-          row_sum = exp_store_row(s, prm.c_scale, -m, tS);  // the same P again for the lanes that kept m
-          l = l * alpha + row_sum;
-          if (j > 0) {  // O holds earlier steps' sums only after the first step
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t o[32];
-              tmem_ld_x32(tO + c0, o);
-#pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              tmem_st_x32(tO + c0, o);
-            }
-          }
-        } else {
-          l += row_sum;
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_p);
       }
+      float m = -INFINITY, l = 0.f;
+      // One pass over this slot's key tiles j0, j0 + dj, ... (instantiated twice below with constant strides, so
+      // that the two-tile path compiles exactly as a plain loop from key tile 0).
+      auto slot_pass = [&](const int j0, const int dj) {
+        for (int j = j0; j < nt; j += dj) {
+          const bool first = j == j0;
+          const int valid = tile_valid(it, j, nt0);
+          ok = mbar_wait(bar_s, s_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          s_n++;
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t sr[128];
+          tmem_ld_x128(tS, sr);
+          float(&s)[128] = *reinterpret_cast<float(*)[128]>(sr);
+          if (valid < kTileRows) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= valid) s[c] = -INFINITY;
+          }
+          // P = 2^(s*c - m) against the current reference m, and its row sum. The reference only has to keep P finite
+          // and within a sane range, not equal the row max: the final normalisation divides by l built against the
+          // same reference. So the exact row max is computed only when this step's sum exceeds 2^16 (or is not
+          // finite; the first step of an item starts from m = -inf): then the warp takes the max, raises m, redoes
+          // the exponentials and rescales l and, after the first step, O.
+          float row_sum = exp_store_row(s, prm.c_scale, -m, tS);
+          const bool need = !(row_sum <= kLazyLimit);
+          if (__any_sync(0xffffffffu, need)) {  // warp-uniform: tcgen05.ld/st are warp-collective
+            float alpha = 1.f;
+            if (need) {
+              // Row max: 8 independent chains of three-input maxima over 16 columns each.
+              float mx[8];
+#pragma unroll
+              for (int a = 0; a < 8; ++a) {
+                mx[a] = fmaxf(s[16 * a], s[16 * a + 15]);
+#pragma unroll
+                for (int c = 1; c < 15; c += 2) mx[a] = max3(mx[a], s[16 * a + c], s[16 * a + c + 1]);
+              }
+              const float m_cand =
+                  fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7])) * prm.c_scale;
+              alpha = first ? 0.f : ex2(m - m_cand);
+              m = m_cand;
+            }
+            row_sum = exp_store_row(s, prm.c_scale, -m, tS);  // the same P again for the lanes that kept m
+            l = l * alpha + row_sum;
+            if (!first) {  // O holds earlier steps' sums only after the first step
+#pragma unroll
+              for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld_x32(tO + c0, o);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                tmem_st_x32(tO + c0, o);
+              }
+            }
+          } else {
+            l += row_sum;
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_p);
+        }
+      };
+      if (alt)
+        slot_pass(t, 2);
+      else
+        slot_pass(0, 1);
       if (!ok) break;
+      if (alt && t == 1) {
+        // Second half of an alternating-key item: hand (m, l) to the first warpgroup, which merges the halves and
+        // waits for O_1 (o_full(1) completes for this item without this warpgroup waiting on it: count it).
+        sts_f2(xchg, m, l);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.xchg_full());
+        xk_n++;
+        o_n++;
+        o1_pending = true;
+        continue;
+      }
       ok = mbar_wait(bar_o, o_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       o_n++;
       if (!ok) break;
+      // Merge weights of the two halves of an alternating-key item: O = (a0 O_0 + a1 O_1) / (a0 l_0 + a1 l_1)
+      // against the larger reference m (log-sum-exp merge); a0 = 1, a1 = 0 otherwise.
+      float a0 = 1.f, a1 = 0.f;
+      if (alt) {
+        ok = mbar_wait(bars.o_full(1), o1_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        o1_n++;
+        if (ok) ok = mbar_wait(bars.xchg_full(), xk_n & 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        xk_n++;
+        if (!ok) break;
+        const float2 ml1 = lds_f2(xchg);
+        const float mm = fmaxf(m, ml1.x);
+        a0 = ex2(m - mm);
+        a1 = ex2(ml1.x - mm);
+        l = a0 * l + a1 * ml1.y;
+        m = mm;
+      }
       tc_fence_after();
+      // O of this row (columns [c0, c0 + 32)): this slot's, or the merge of both slots' for alternating keys
+      const uint32_t tO1 = tmem + lane_base + C::kTmemO + 128;
+      auto load_o = [&](int c0, uint32_t (&o)[32]) {
+        tmem_ld_x32(tO + c0, o);
+        if (alt) {
+          uint32_t o1[32];
+          tmem_ld_x32(tO1 + c0, o1);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            o[c] = __float_as_uint(fmaf(a1, __uint_as_float(o1[c]), a0 * __uint_as_float(o[c])));
+        }
+      };
       // Epilogue: O / l, straight into this row's place (no scatter pass).
       const int row = it.q_lo + t * kTileRows + row_in_tile;
       const bool row_ok = row < it.q_hi;
@@ -539,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t o[32];
-            tmem_ld_x32(tO + half * 64 + c0, o);
+            load_o(half * 64 + c0, o);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {  // 16-byte chunk c of the row sits at chunk c ^ (row % 8)
               const int c = c0 / 8 + q;
@@ -572,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
-          tmem_ld_x32(tO + c0, o);
+          load_o(c0, o);
           uint32_t w[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c)
@@ -592,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
-          tmem_ld_x32(tO + c0, o);
+          load_o(c0, o);
           if (row_ok) {
             float4* d4 = reinterpret_cast<float4*>(dst + c0);
 #pragma unroll
@@ -604,6 +717,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_ok) prm.ws_lse[slot] = m + __log2f(l);
       }
       tc_fence_before();
+      if (alt) {  // O_1 and the exchange have been read (tcgen05.ld waits are in the loads): slot 1 may move on
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.o1_free());
+      }
     }
     // The warpgroup's last stores must have written out (and read their stage) before the CTA leaves.
     if (C::kStage && (warp & 3) == 0 && lane == 0) bulk_wait();
