@@ -541,9 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P = 2^(s*c - m) against the current reference m, and its row sum. The reference only has to keep P finite
           // and within a sane range, not equal the row max: the final normalisation divides by l built against the
           // same reference. So the exact row max is computed only when this step's sum exceeds 2^16 (or is not
-          // finite; the first step of an item starts from m = -inf): then the warp takes the max, raises m, redoes
-          // the exponentials and rescales l and, after the first step, O.
-          float row_sum = exp_store_row(s, prm.c_scale, -m, tS);
+          // finite): then the warp takes the max, raises m, redoes the exponentials and rescales l and, after the
+          // first step, O. The first step starts from m = -inf, so it takes the exact max straight away.
+          float row_sum = first ? INFINITY : exp_store_row(s, prm.c_scale, -m, tS);
           const bool need = !(row_sum <= kLazyLimit);
           if (__any_sync(0xffffffffu, need)) {  // warp-uniform: tcgen05.ld/st are warp-collective
             float alpha = 1.f;
@@ -639,30 +639,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = it.bh / prm.H, h = it.bh % prm.H;
       const int row0 = it.q_lo + t * kTileRows;
       if (C::kStage && it.split < 0 && row0 + kTileRows <= it.q_hi) {
-        // A full tile: each 64-column half is written to this tile's stage in the store's 128-byte swizzle, then
-        // one thread of the warpgroup stores it with TMA once all four warps have written their rows.
+        // A full tile: each 64-column half is packed in registers, written to this tile's stage in the store's
+        // 128-byte swizzle, and stored with TMA by one thread of the warpgroup once all four warps have written
+        // their rows. That thread waits for the copy engine to have read a half from the stage only when the stage
+        // is needed again (for the next half, or in the next full-tile epilogue), so the read overlaps the TMEM
+        // loads of what comes next.
         const uint32_t stage = s_base + C::kStageOff + t * C::kStageTileBytes;
         const bool issuer = (warp & 3) == 0 && lane == 0;
 #pragma unroll 1
         for (int half = 0; half < 2 && ok; ++half) {
-          ok = mbar_wait(bars.stage_free(t), (st_n & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          const uint32_t row_addr = stage + row_in_tile * 128;
+          uint32_t pk[32];  // the half's 64 columns of this row as bf16 pairs
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t o[32];
             load_o(half * 64 + c0, o);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 16-byte chunk c of the row sits at chunk c ^ (row % 8)
-              const int c = c0 / 8 + q;
-              sts_u4(row_addr + ((c ^ (row_in_tile & 7)) << 4),
-                     pack_bf16(__uint_as_float(o[8 * q]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l),
-                     pack_bf16(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l),
-                     pack_bf16(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l),
-                     pack_bf16(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l));
-            }
+            for (int c = 0; c < 16; ++c)
+              pk[c0 / 2 + c] = pack_bf16(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
           }
+          if (issuer && st_n > 0) {  // the previous store out of this stage (this tile's or an earlier one's)
+            bulk_wait_read();
+            mbar_arrive(bars.stage_free(t));
+          }
+          ok = mbar_wait(bars.stage_free(t), (st_n & 1) ^ 1, abort_flag, err, kErrTimeout, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          const uint32_t row_addr = stage + row_in_tile * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)  // 16-byte chunk c of the row sits at chunk c ^ (row % 8)
+            sts_u4(row_addr + ((c ^ (row_in_tile & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bars.stage_full(t));
@@ -671,8 +676,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
               tma_store_4d(&tmap_o, stage, half * 64, h, row0, b);
               bulk_commit();
-              bulk_wait_read();
-              mbar_arrive(bars.stage_free(t));
             }
           }
           ok = __all_sync(0xffffffffu, ok);
