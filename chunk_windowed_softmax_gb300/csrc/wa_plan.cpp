@@ -61,6 +61,7 @@ struct wa_plan {
   std::vector<int> pc_item_off;                  // launch p: items [pc_item_off[p], pc_item_off[p + 1])
   cudaStream_t s_in = nullptr, s_out = nullptr, s_c2 = nullptr;
   std::vector<cudaEvent_t> pc_ev;                // per piece: copies in, launch done; then four for the whole call
+  bool host_ready = false;                       // all of the above set up (a failed set-up leaves none of it)
 };
 
 namespace wa {
@@ -423,7 +424,8 @@ void free_plan(wa_plan* p) {
   if (p->d_bws) cudaFree(p->d_bws);
   if (p->d_stage) cudaFree(p->d_stage);
   if (p->d_items_pc) cudaFree(p->d_items_pc);
-  for (cudaEvent_t e : p->pc_ev) cudaEventDestroy(e);
+  for (cudaEvent_t e : p->pc_ev)
+    if (e) cudaEventDestroy(e);
   if (p->s_in) cudaStreamDestroy(p->s_in);
   if (p->s_out) cudaStreamDestroy(p->s_out);
   if (p->s_c2) cudaStreamDestroy(p->s_c2);
@@ -803,9 +805,27 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
 
 namespace {
 
-// Lazily set up what wa_forward_host needs; called with plan->mu held.
+// Undo a partial set-up of the host path: the next wa_forward_host starts it again from nothing.
+void release_host_path(wa_plan_t* plan) {
+  for (cudaEvent_t& ev : plan->pc_ev)
+    if (ev) cudaEventDestroy(ev);
+  plan->pc_ev.clear();
+  for (cudaStream_t* st : {&plan->s_in, &plan->s_out, &plan->s_c2}) {
+    if (*st) cudaStreamDestroy(*st);
+    *st = nullptr;
+  }
+  if (plan->d_items_pc) cudaFree(plan->d_items_pc);
+  plan->d_items_pc = nullptr;
+  if (plan->d_stage) cudaFree(plan->d_stage);
+  plan->d_stage = nullptr;
+  cudaGetLastError();  // clear a non-sticky error of the failed step
+}
+
+// Lazily set up what wa_forward_host needs; called with plan->mu held. All or nothing: the host tables are built
+// first (a failed host allocation throws before anything exists on the device), then every device resource; if one
+// of those fails, everything set up so far is released.
 wa_status prepare_host_path(wa_plan_t* plan, size_t span_bytes) {
-  if (plan->d_stage) return WA_OK;
+  if (plan->host_ready) return WA_OK;
   wa::build_host_schedule(plan->hp, &plan->hs);
   const int n_pieces = (int)plan->hs.pieces.size();
   std::vector<std::vector<wa::Item>> by_launch(n_pieces);
@@ -818,25 +838,25 @@ wa_status prepare_host_path(wa_plan_t* plan, size_t span_bytes) {
     regrouped.insert(regrouped.end(), by_launch[p].begin(), by_launch[p].end());
     plan->pc_item_off[p + 1] = (int)regrouped.size();
   }
+  plan->pc_ev.assign(3 * n_pieces + 4, nullptr);
   cudaError_t e = dev_alloc(&plan->d_stage, 4 * span_bytes);
   if (e == cudaSuccess) e = dev_alloc(&plan->d_items_pc, std::max<size_t>(1, regrouped.size()) * sizeof(wa::Item));
   if (e != cudaSuccess) {
-    cudaGetLastError();
-    if (plan->d_stage) cudaFree(plan->d_stage);
-    plan->d_stage = nullptr;
-    if (plan->d_items_pc) cudaFree(plan->d_items_pc);
-    plan->d_items_pc = nullptr;
+    release_host_path(plan);
     return e == cudaErrorMemoryAllocation ? WA_ERR_OOM : WA_ERR_CUDA;
   }
-  if (cudaMemcpy(plan->d_items_pc, regrouped.data(), regrouped.size() * sizeof(wa::Item), cudaMemcpyHostToDevice) !=
-          cudaSuccess ||
-      cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&plan->s_c2, cudaStreamNonBlocking) != cudaSuccess)
-    return WA_ERR_CUDA;
-  plan->pc_ev.resize(3 * n_pieces + 4);
+  bool ok = cudaMemcpy(plan->d_items_pc, regrouped.data(), regrouped.size() * sizeof(wa::Item),
+                       cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&plan->s_c2, cudaStreamNonBlocking) == cudaSuccess;
   for (cudaEvent_t& ev : plan->pc_ev)
-    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return WA_ERR_CUDA;
+    ok = ok && cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    release_host_path(plan);
+    return WA_ERR_CUDA;
+  }
+  plan->host_ready = true;
   return WA_OK;
 }
 

@@ -194,7 +194,7 @@ void wa_plan_release(wa_plan_t* plan);
  * Host-only: the plan a geometry would get, without touching any device. Fills `info`; when `groups` is not
  * NULL writes min(n_groups, groups_cap) group rows; when `items` is not NULL writes min(n_items, items_cap)
  * work items, 8 int64 each: {b*H + h, kind (0 window, 1 global split), q_lo, q_hi, kv0_lo, kv0_hi, kv1_lo,
- * kv1_hi}. Errors: as wa_plan_create for the arguments; never WA_ERR_OOM/WA_ERR_CUDA.
+ * kv1_hi}. Errors: as wa_plan_create for the arguments; WA_ERR_OOM if host memory runs out; never WA_ERR_CUDA.
  */
 wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, wa_plan_info_t* info,
                                wa_group_t* groups, int64_t groups_cap, int64_t* items, int64_t items_cap);
@@ -237,7 +237,8 @@ const char* wa_status_string(wa_status s);
  *   calls on one stream are ordered. The array keeps the previous call's contents; the call clears what must
  *   start at zero.
  * Errors: as wa_forward; WA_ERR_UNSUPPORTED, before anything is launched, when the geometry's scratch (work list
- * + B*H*G*n_splits*(D+1)*4 bytes of workspace) exceeds the 32 MiB array. Device-side watchdog failures are latched
+ * + B*H*G*n_splits*(D+1)*4 bytes of workspace) exceeds the 32 MiB array; WA_ERR_OOM if the host-side work list
+ * cannot be built (host memory). Device-side watchdog failures are latched
  * in the array's error word and cleared by the next call; this entry point does not report them.
  */
 wa_status wa_forward_static(int T, int S, int K, int r, int G, const wa_layout_t* layout, const void* q,

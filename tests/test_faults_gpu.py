@@ -78,3 +78,26 @@ def test_forward_argument_errors(cuda):
         assert plan.check_error() == 0
     finally:
         plan.close()
+
+
+def test_failed_host_path_set_up_is_undone_and_retried(cuda):
+    # the host-buffer forward sets up its device copies on first use; a failed allocation there must leave nothing
+    # half set up, so that the next call sets it up again and gives the plain forward's result
+    w = configs.Workload("host_retry", B=1, H=2, D=128, T=6, S=100, K=2, r=1, G=40, global_pos=0, seed=91)
+    q, k, v = inputs.make_qkv(w)
+    plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
+    try:
+        want = plan.forward(q.cuda(), k.cuda(), v.cuda()).cpu()
+        os.environ["WA_TEST_FAIL_ALLOC"] = "1"
+        try:
+            with pytest.raises(cuda.WAError) as e:
+                plan.forward_host(q, k, v)
+            assert e.value.status == 3  # WA_ERR_OOM
+        finally:
+            del os.environ["WA_TEST_FAIL_ALLOC"]
+        for _ in range(2):
+            got = plan.forward_host(q, k, v)
+            assert torch.equal(got, want)
+        assert plan.check_error() == 0
+    finally:
+        plan.close()
