@@ -116,7 +116,8 @@ extern "C" wa_status wa_forward_static(int T, int S, int K, int r, int G, const 
         cudaGetLastError();
         return WA_ERR_CUDA;
       }
-      if (ctx != 0) g_scratch_addr.emplace_back(ctx, base);  // context unknown: look it up on every call
+      if (ctx != 0)  // context unknown (or no room to remember it): look it up on every call
+        wa::host_tables([&] { g_scratch_addr.emplace_back(ctx, base); });
     }
   }
   unsigned char* b = static_cast<unsigned char*>(base);
@@ -129,7 +130,12 @@ extern "C" wa_status wa_forward_static(int T, int S, int K, int r, int G, const 
   // The array keeps the previous call's contents: the first expansion launch clears the error word; the work list
   // is rewritten in full; every workspace entry the merge reads is written by the attention kernel first.
   {
-    std::vector<int> run_lo(n_tpl), run_hi(n_tpl);  // the run of equal key-tile counts each template belongs to
+    std::vector<int> run_lo, run_hi;  // the run of equal key-tile counts each template belongs to
+    if (wa::host_tables([&] {
+          run_lo.resize(n_tpl);
+          run_hi.resize(n_tpl);
+        }) != WA_OK)
+      return WA_ERR_OOM;
     auto tiles = [](const wa::Item& it) {
       auto seg = [](int lo, int hi) { return hi > lo ? (hi - lo + wa::kTileRows - 1) / wa::kTileRows : 0; };
       return seg(it.s0_lo, it.s0_hi) + seg(it.s1_lo, it.s1_hi);

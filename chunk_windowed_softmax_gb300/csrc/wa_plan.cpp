@@ -609,10 +609,9 @@ wa_status wa_plan_create(int T, int S, int K, int r, int G, const wa_layout_t* l
     g_cache.remove(victim);
     free_plan(victim);
   }
-  if (g_cache.size() < kMaxCached) {
+  if (g_cache.size() < kMaxCached &&
+      wa::host_tables([&] { g_cache.push_back(p); }) == WA_OK)  // else the plan stays uncached
     p->cached = true;
-    g_cache.push_back(p);
-  }
   *out = p;
   return WA_OK;
 }
@@ -694,7 +693,10 @@ wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void
     while ((int)plan->prof_ev.size() < 3 * (plan->prof_n + 1)) {
       cudaEvent_t e;
       if (cudaEventCreate(&e) != cudaSuccess) return WA_ERR_CUDA;
-      plan->prof_ev.push_back(e);
+      if (wa::host_tables([&] { plan->prof_ev.push_back(e); }) != WA_OK) {
+        cudaEventDestroy(e);
+        return WA_ERR_OOM;
+      }
     }
     ev = &plan->prof_ev[3 * plan->prof_n++];
   }
@@ -792,7 +794,10 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
     while ((int)plan->bprof_ev.size() < 5 * (plan->bprof_n + 1)) {
       cudaEvent_t e;
       if (cudaEventCreate(&e) != cudaSuccess) return WA_ERR_CUDA;
-      plan->bprof_ev.push_back(e);
+      if (wa::host_tables([&] { plan->bprof_ev.push_back(e); }) != WA_OK) {
+        cudaEventDestroy(e);
+        return WA_ERR_OOM;
+      }
     }
     ev = reinterpret_cast<void* const*>(&plan->bprof_ev[5 * plan->bprof_n++]);
   }
