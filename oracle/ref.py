@@ -12,11 +12,13 @@ What is computed (the VDN-Minimax-H3 window-attention article, lqnn.cn):
   * section 三 (the decomposed idea): the result is mathematically identical to the masked kernel: each query's
     softmax is normalised over exactly its kept set; the article keeps an eager per-frame loop as the
     correctness baseline, which is the shape of ``window_attention`` below.
-Readings where the article is silent (each one is listed with its reason in the design notes):
-  * chunks past either end of the sequence do not exist: the window is clamped, not shifted;
-  * T need not be a multiple of K: the last chunk is partial and otherwise ordinary;
-  * globals sit after the frame tokens (global_pos = 0) or before them (global_pos = 1);
-  * scores are scaled by 1/sqrt(D); non-causal; no bias, softcap or dropout.
+Readings where the article is silent, each the plainest one the rest of the article supports:
+  * chunks past either end of the sequence do not exist: the window is clamped, not shifted (section 一 speaks of
+    the whole chunks in the range, i.e. the ones that exist);
+  * T need not be a multiple of K: the last chunk is partial and otherwise ordinary (every K frames form a chunk);
+  * globals sit after the frame tokens (global_pos = 0) or before them (global_pos = 1); either placement gives the
+    same result up to that permutation of the rows;
+  * scores are scaled by 1/sqrt(D); non-causal; no bias, softcap or dropout (the article mentions none).
 
 The backward (window_attention_backward, row_logsumexp) follows the same loop and is pinned by
 tests/test_oracle_backward.py: central finite differences of the forward above, and torch autograd through a
