@@ -709,12 +709,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
           load_o(c0, o);
-          if (row_ok) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c0);
+          if (row_ok) {  // 32-byte stores: each fills a whole sector of the row
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              d4[c] = make_float4(__uint_as_float(o[4 * c]) * inv_l, __uint_as_float(o[4 * c + 1]) * inv_l,
-                                  __uint_as_float(o[4 * c + 2]) * inv_l, __uint_as_float(o[4 * c + 3]) * inv_l);
+            for (int c = 0; c < 4; ++c) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * c + e]) * inv_l;
+              asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + c0 + 8 * c),
+                           "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7])
+                           : "memory");
+            }
           }
         }
         if (row_ok) prm.ws_lse[slot] = m + __log2f(l);
