@@ -193,17 +193,21 @@ void build_host_plan(const Geometry& g, HostPlan* hp) {
     hp->groups.push_back(gr);
   }
   // Split count of the global leg: splits about as long as the longest window item, so that every item of the
-  // persistent kernel costs about the same; twice that when the global rows fill at least four items' query tile
-  // pairs per head, since their split items are then plentiful and longer splits mean fewer item switches and a
-  // smaller merge (measured at 56 heads x 99,968 rows, 2,048 global rows: forward -0.8 %, backward -1.0 %; with 77
-  // global rows, one partly filled query tile per head, the longer splits made the forward 1.6 % slower).
+  // persistent kernel costs about the same; four times that when the global rows fill at least four items' query
+  // tile pairs per head, since their split items are then plentiful, are claimed first (longest first) and leave
+  // the window items to even out the finish, and longer splits mean fewer item switches (a split item's switch is
+  // about four times a window item's: it writes fp32 partial rows) and a smaller merge. Measured at 56 heads x
+  // 99,968 rows, 2,048 global rows: twice the window item against once, forward -0.8 %, backward -1.0 %; four
+  // times against twice, forward -0.3 %, the backward unchanged, and -2.1 to -2.4 % on the same shape with one-frame
+  // chunks and r = 0. With 77 global rows, one partly filled query tile per head, longer splits made the forward
+  // 1.6 % slower.
   int64_t wmax = 1;
   for (auto& gr : hp->groups) wmax = std::max(wmax, seg_tiles(gr.kv0_lo, gr.kv0_hi) + seg_tiles(gr.kv1_lo, gr.kv1_hi));
   int64_t Lt = cdiv(g.L, kTileRows);
   int n_splits = 1;
   int64_t tps = Lt;
   if (g.G > 0) {
-    const int64_t split_tiles = g.G >= 4 * kItemRows ? 2 * wmax : wmax;
+    const int64_t split_tiles = g.G >= 4 * kItemRows ? 4 * wmax : wmax;
     int64_t p = std::min<int64_t>(64, std::max<int64_t>(1, cdiv(Lt, split_tiles)));
     tps = cdiv(Lt, p);
     n_splits = (int)cdiv(Lt, tps);
