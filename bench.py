@@ -389,6 +389,66 @@ def run_backward(args, w):
         "gpu_launches": (3 + (1 if w.G > 0 else 0)) * args.steps, "clocks": clocks}), flush=True)
 
 
+def secondary_paths(w, q, k, v, plan, bf16_peak, steps=10):
+    """Short measurements of the e4m3 forward and of the backward on the default workload, taken after the timed
+    forward region (so they change neither its value nor its clock record) and reported beside the main line. Each
+    is a few warm-up calls and `steps` timed calls with CUDA events on the current stream; a failure is reported as
+    an error string instead of a number."""
+    import torch
+    out = {}
+    stream = torch.cuda.current_stream()
+    info = plan.info()
+    pairs = info["kept_pairs"] * w.B * w.H
+    flops = 4.0 * w.D * pairs
+    try:
+        sq = float(q.float().abs().max()) / 448.0
+        sk = float(k.float().abs().max()) / 448.0
+        q8 = (q.float() / sq).to(torch.float8_e4m3fn)
+        k8 = (k.float() / sk).to(torch.float8_e4m3fn)
+        o8 = torch.empty_like(v)
+        for _ in range(3):
+            plan.forward_fp8(q8, k8, v, sq, sk, out=o8)
+        plan.profile(True)
+        ms, _ = timed_steps(lambda: plan.forward_fp8(q8, k8, v, sq, sk, out=o8), steps, stream, q.device,
+                            q8.numel() * 2 + v.numel() * 4)
+        attn, _, n = plan.profile_read()
+        plan.profile(False)
+        st = plan.check_error()
+        kms = attn / max(1, n)
+        mixed = bf16_peak * 4.0 / 3.0
+        out["e4m3_forward"] = {"ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                               "kernel_ms": kms, "frac": flops / (kms * 1e-3) / 1e12 / mixed, "peak": mixed,
+                               "steps": steps, "status": st}
+        del q8, k8, o8
+    except Exception as e:  # noqa: BLE001 -- reported in the line, never fatal for the main measurement
+        out["e4m3_forward"] = {"error": str(e)[:200]}
+    try:
+        from chunk_windowed_softmax_gb300 import inputs
+        dout = inputs.make_dout(w, device=q.device)
+        o, lse = plan.forward_lse(q, k, v)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        for _ in range(2):
+            plan.backward(q, k, v, o, dout, lse, dq, dk, dv)
+        plan.profile(True)
+        ms, _ = timed_steps(lambda: plan.backward(q, k, v, o, dout, lse, dq, dk, dv), max(3, steps // 2), stream,
+                            q.device, 8 * q.numel() * 2)
+        kms, n = plan.profile_read_backward()
+        plan.profile(False)
+        st = plan.check_error()
+        kms = [x / max(1, n) for x in kms]
+        dkdv = 8.0 * w.D * pairs / (kms[2] * 1e-3) / 1e12
+        dqk = 6.0 * w.D * pairs / (kms[1] * 1e-3) / 1e12
+        out["backward"] = {"ms_per_step": ms, "value": 10.0 * w.D * pairs / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                           "kernels_ms": {"row_dots": kms[0], "dq": kms[1], "dk_dv": kms[2], "split_sums": kms[3]},
+                           "frac": {"dq": dqk / bf16_peak, "dk_dv": dkdv / bf16_peak}, "peak": bf16_peak,
+                           "steps": max(3, steps // 2), "status": st}
+        del dout, o, lse, dq, dk, dv
+    except Exception as e:  # noqa: BLE001
+        out["backward"] = {"error": str(e)[:200]}
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_head_sharded(args, w, rank, world, local):
     """One layer sharded by heads across the ranks: each rank starts from its shard of the packed sequence (all
     heads), q, k and v go to head shards by all-to-all, each rank computes its H/N heads over the whole sequence with
@@ -562,6 +622,9 @@ def main():
         if world > 1:
             dist.destroy_process_group()
         return
+    # The e4m3 forward and the backward, measured briefly on the same workload after the timed region (single
+    # process only: a multi-GPU run times the forward replicas alone).
+    secondary = secondary_paths(w, q, k, v, plan, bf16_peak) if world == 1 else None
     # End to end through the public call with host tensors: pinned host -> device copies, the forward, and the
     # device -> host copy of the result, every step.
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
@@ -612,6 +675,9 @@ def main():
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
+        if secondary is not None:
+            res["secondary"] = dict(secondary, note="measured after the timed region, not part of value; "
+                                                    "clocks not sampled")
         print(json.dumps(res), flush=True)
     plan.close()
     if world > 1:
