@@ -87,8 +87,8 @@ def lib():
         L.wa_geometry_describe.restype = ctypes.c_int
         i64p, i32p = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
         L.wa_host_schedule_describe.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(wa_layout_t), i64p,
-                                                                      ctypes.c_int64, i32p, ctypes.c_int64, i64p,
-                                                                      ctypes.c_int64, i64p, i64p, i32p]
+                                                                      ctypes.c_int64, i64p, i32p, ctypes.c_int64,
+                                                                      i64p, ctypes.c_int64, i64p, i64p, i64p, i32p]
         L.wa_host_schedule_describe.restype = ctypes.c_int
         L.wa_status_string.argtypes = [ctypes.c_int]
         L.wa_status_string.restype = ctypes.c_char_p
@@ -189,24 +189,25 @@ def wa_geometry_describe(T, S, K, r, G, layout, with_groups=True, with_items=Fal
     return info.as_dict(), groups, items
 
 
-def wa_host_schedule_describe(T, S, K, r, G, layout, n_items):
+def wa_host_schedule_describe(T, S, K, r, G, layout):
     """Host-only piece schedule of the host-buffer forward: {"row_pieces": bool, "pieces": [(lo, hi, h_lo, h_hi)] in
-    copy order, "item_launch": [launch per work item, in wa_geometry_describe's item order],
+    copy order, "items": [the host path's work items, as wa_geometry_describe's], "item_launch": [launch per item],
     "out": [(launch, lo, hi, h_lo, h_hi)]}."""
     L = lib()
-    n_pieces, n_out, rows = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    n_pieces, n_items, n_out, rows = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
     args = (T, S, K, r, G, ctypes.byref(layout))
-    _check(L.wa_host_schedule_describe(*args, None, 0, None, 0, None, 0, ctypes.byref(n_pieces), ctypes.byref(n_out),
-                                       ctypes.byref(rows)), "wa_host_schedule_describe")
+    counts = (ctypes.byref(n_pieces), ctypes.byref(n_items), ctypes.byref(n_out), ctypes.byref(rows))
+    _check(L.wa_host_schedule_describe(*args, None, 0, None, None, 0, None, 0, *counts), "wa_host_schedule_describe")
     pbuf = (ctypes.c_int64 * (4 * max(1, n_pieces.value)))()
-    lbuf = (ctypes.c_int32 * max(1, n_items))()
+    ibuf = (ctypes.c_int64 * (8 * max(1, n_items.value)))()
+    lbuf = (ctypes.c_int32 * max(1, n_items.value))()
     obuf = (ctypes.c_int64 * (5 * max(1, n_out.value)))()
-    _check(L.wa_host_schedule_describe(*args, pbuf, n_pieces.value, lbuf, n_items, obuf, n_out.value,
-                                       ctypes.byref(n_pieces), ctypes.byref(n_out), ctypes.byref(rows)),
-           "wa_host_schedule_describe")
+    _check(L.wa_host_schedule_describe(*args, pbuf, n_pieces.value, ibuf, lbuf, n_items.value, obuf, n_out.value,
+                                       *counts), "wa_host_schedule_describe")
     return {"row_pieces": bool(rows.value),
             "pieces": [tuple(pbuf[4 * i:4 * i + 4]) for i in range(n_pieces.value)],
-            "item_launch": list(lbuf[:n_items]),
+            "items": [tuple(ibuf[8 * i:8 * i + 8]) for i in range(n_items.value)],
+            "item_launch": list(lbuf[:n_items.value]),
             "out": [tuple(obuf[5 * i:5 * i + 5]) for i in range(n_out.value)]}
 
 

@@ -59,8 +59,12 @@ struct HostSchedule {
 
 // Validate arguments; on success fill `geo`.
 wa_status make_geometry(int T, int S, int K, int r, int G, const wa_layout_t* layout, Geometry* geo);
+// Key splits of the global leg, in multiples of the longest window item (when the global rows are plentiful): the
+// device plans' work list, and the host-buffer forward's own list (which keeps the last split short).
+constexpr int kDeviceSplitMult = 4;
+constexpr int kHostSplitMult = 2;
 // Build groups, splits and the ordered work list on the host.
-void build_host_plan(const Geometry& geo, HostPlan* hp);
+void build_host_plan(const Geometry& geo, HostPlan* hp, int split_mult = kDeviceSplitMult);
 // Build the host-buffer forward's piece schedule for a plan (host only).
 void build_host_schedule(const HostPlan& hp, HostSchedule* hs);
 // Run `build` (which fills host-side tables) so that no C++ exception leaves the C ABI: a failed host allocation

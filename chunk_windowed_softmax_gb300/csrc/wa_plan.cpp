@@ -61,6 +61,9 @@ struct wa_plan {
   std::vector<int> pc_item_off;                  // launch p: items [pc_item_off[p], pc_item_off[p + 1])
   cudaStream_t s_in = nullptr, s_out = nullptr, s_c2 = nullptr;
   std::vector<cudaEvent_t> pc_ev;                // per piece: copies in, launch done; then four for the whole call
+  wa::HostPlan hp_host;                          // the work list of the host path (its own global key splits)
+  float* d_ws_host = nullptr;                    // its global-leg workspace: partial outputs, then log-sum-exp
+  int64_t ws_o_elems_host = 0;
   bool host_ready = false;                       // all of the above set up (a failed set-up leaves none of it)
 };
 
@@ -161,7 +164,7 @@ wa_status make_geometry(int T, int S, int K, int r, int G, const wa_layout_t* la
 
 static int64_t seg_tiles(int64_t lo, int64_t hi) { return hi > lo ? cdiv(hi - lo, kTileRows) : 0; }
 
-void build_host_plan(const Geometry& g, HostPlan* hp) {
+void build_host_plan(const Geometry& g, HostPlan* hp, int split_mult) {
   const int64_t KS = (int64_t)g.K * g.S;
   hp->geo = g;
   hp->groups.clear();
@@ -193,21 +196,23 @@ void build_host_plan(const Geometry& g, HostPlan* hp) {
     hp->groups.push_back(gr);
   }
   // Split count of the global leg: splits about as long as the longest window item, so that every item of the
-  // persistent kernel costs about the same; four times that when the global rows fill at least four items' query
-  // tile pairs per head, since their split items are then plentiful, are claimed first (longest first) and leave
-  // the window items to even out the finish, and longer splits mean fewer item switches (a split item's switch is
-  // about four times a window item's: it writes fp32 partial rows) and a smaller merge. Measured at 56 heads x
-  // 99,968 rows, 2,048 global rows: twice the window item against once, forward -0.8 %, backward -1.0 %; four
-  // times against twice, forward -0.3 %, the backward unchanged, and -2.1 to -2.4 % on the same shape with one-frame
-  // chunks and r = 0. With 77 global rows, one partly filled query tile per head, longer splits made the forward
-  // 1.6 % slower.
+  // persistent kernel costs about the same; split_mult times that when the global rows fill at least four items'
+  // query tile pairs per head, since their split items are then plentiful, are claimed first (longest first) and
+  // leave the window items to even out the finish, and longer splits mean fewer item switches (a split item's
+  // switch is about four times a window item's: it writes fp32 partial rows) and a smaller merge. Measured at 56
+  // heads x 99,968 rows, 2,048 global rows: twice the window item against once, forward -0.8 %, backward -1.0 %;
+  // four times against twice (the device plan's kDeviceSplitMult), forward -0.3 %, the backward unchanged, and
+  // -2.1 to -2.4 % on the same shape with one-frame chunks and r = 0. The host-buffer forward keeps twice
+  // (kHostSplitMult): it can run a split only once every row of its key range has arrived, so a longer last split
+  // leaves more work after the last copy (four times: 1.6-1.9 % slower there). With 77 global rows, one partly
+  // filled query tile per head, longer splits made the forward 1.6 % slower.
   int64_t wmax = 1;
   for (auto& gr : hp->groups) wmax = std::max(wmax, seg_tiles(gr.kv0_lo, gr.kv0_hi) + seg_tiles(gr.kv1_lo, gr.kv1_hi));
   int64_t Lt = cdiv(g.L, kTileRows);
   int n_splits = 1;
   int64_t tps = Lt;
   if (g.G > 0) {
-    const int64_t split_tiles = g.G >= 4 * kItemRows ? 4 * wmax : wmax;
+    const int64_t split_tiles = g.G >= 4 * kItemRows ? split_mult * wmax : wmax;
     int64_t p = std::min<int64_t>(64, std::max<int64_t>(1, cdiv(Lt, split_tiles)));
     tps = cdiv(Lt, p);
     n_splits = (int)cdiv(Lt, tps);
@@ -428,6 +433,7 @@ void free_plan(wa_plan* p) {
   if (p->d_bws) cudaFree(p->d_bws);
   if (p->d_stage) cudaFree(p->d_stage);
   if (p->d_items_pc) cudaFree(p->d_items_pc);
+  if (p->d_ws_host) cudaFree(p->d_ws_host);
   for (cudaEvent_t e : p->pc_ev)
     if (e) cudaEventDestroy(e);
   if (p->s_in) cudaStreamDestroy(p->s_in);
@@ -459,7 +465,7 @@ wa_status create_uncached(const wa::Geometry& g, int dev, wa_plan** out) {
   wa_plan* p = new (std::nothrow) wa_plan();
   if (!p) return WA_ERR_OOM;
   p->device = dev;
-  if (wa::host_tables([&] { wa::build_host_plan(g, &p->hp); }) != WA_OK) {
+  if (wa::host_tables([&] { wa::build_host_plan(g, &p->hp, wa::kDeviceSplitMult); }) != WA_OK) {
     delete p;
     return WA_ERR_OOM;
   }
@@ -525,7 +531,7 @@ wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layou
   wa_status st = wa::make_geometry(T, S, K, r, G, layout, &g);
   if (st != WA_OK) return st;
   wa::HostPlan hp;
-  st = wa::host_tables([&] { wa::build_host_plan(g, &hp); });
+  st = wa::host_tables([&] { wa::build_host_plan(g, &hp, wa::kDeviceSplitMult); });
   if (st != WA_OK) return st;
   *info = hp.info;
   if (groups)
@@ -541,20 +547,22 @@ wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layou
 }
 
 wa_status wa_host_schedule_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, int64_t* pieces,
-                                    int64_t pieces_cap, int32_t* item_launch, int64_t items_cap, int64_t* out_ranges,
-                                    int64_t out_cap, int64_t* n_pieces, int64_t* n_out, int32_t* row_pieces) {
-  if (!n_pieces || !n_out || !row_pieces) return WA_ERR_INVALID;
+                                    int64_t pieces_cap, int64_t* items, int32_t* item_launch, int64_t items_cap,
+                                    int64_t* out_ranges, int64_t out_cap, int64_t* n_pieces, int64_t* n_items,
+                                    int64_t* n_out, int32_t* row_pieces) {
+  if (!n_pieces || !n_items || !n_out || !row_pieces) return WA_ERR_INVALID;
   wa::Geometry g;
   wa_status st = wa::make_geometry(T, S, K, r, G, layout, &g);
   if (st != WA_OK) return st;
   wa::HostPlan hp;
   wa::HostSchedule hs;
   st = wa::host_tables([&] {
-    wa::build_host_plan(g, &hp);
+    wa::build_host_plan(g, &hp, wa::kHostSplitMult);
     wa::build_host_schedule(hp, &hs);
   });
   if (st != WA_OK) return st;
   *n_pieces = (int64_t)hs.pieces.size();
+  *n_items = (int64_t)hp.items.size();
   *row_pieces = hs.rows ? 1 : 0;
   if (pieces)
     for (int64_t i = 0; i < std::min<int64_t>(pieces_cap, *n_pieces); ++i) {
@@ -562,8 +570,15 @@ wa_status wa_host_schedule_describe(int T, int S, int K, int r, int G, const wa_
       int64_t* o = pieces + 4 * i;
       o[0] = pc.lo; o[1] = pc.hi; o[2] = pc.h_lo; o[3] = pc.h_hi;
     }
-  if (item_launch)
-    for (int64_t i = 0; i < std::min<int64_t>(items_cap, (int64_t)hs.launch.size()); ++i) item_launch[i] = hs.launch[i];
+  for (int64_t i = 0; i < std::min<int64_t>(items_cap, *n_items); ++i) {
+    const wa::Item& it = hp.items[i];
+    if (items) {
+      int64_t* o = items + 8 * i;
+      o[0] = it.bh; o[1] = it.split < 0 ? 0 : 1; o[2] = it.q_lo; o[3] = it.q_hi;
+      o[4] = it.s0_lo; o[5] = it.s0_hi; o[6] = it.s1_lo; o[7] = it.s1_hi;
+    }
+    if (item_launch) item_launch[i] = hs.launch[i];
+  }
   int64_t n = 0;
   for (size_t p = 0; p < hs.out.size(); ++p)
     for (const auto* list : {&hs.out[p], &hs.merge[p]})
@@ -827,6 +842,8 @@ void release_host_path(wa_plan_t* plan) {
   plan->d_items_pc = nullptr;
   if (plan->d_stage) cudaFree(plan->d_stage);
   plan->d_stage = nullptr;
+  if (plan->d_ws_host) cudaFree(plan->d_ws_host);
+  plan->d_ws_host = nullptr;
   cudaGetLastError();  // clear a non-sticky error of the failed step
 }
 
@@ -835,21 +852,27 @@ void release_host_path(wa_plan_t* plan) {
 // of those fails, everything set up so far is released.
 wa_status prepare_host_path(wa_plan_t* plan, size_t span_bytes) {
   if (plan->host_ready) return WA_OK;
-  wa::build_host_schedule(plan->hp, &plan->hs);
+  wa::build_host_plan(plan->hp.geo, &plan->hp_host, wa::kHostSplitMult);
+  const wa::HostPlan& hh = plan->hp_host;
+  wa::build_host_schedule(hh, &plan->hs);
   const int n_pieces = (int)plan->hs.pieces.size();
   std::vector<std::vector<wa::Item>> by_launch(n_pieces);
-  for (size_t i = 0; i < plan->hp.items.size(); ++i)  // keeps the longest-first order inside each launch
-    by_launch[plan->hs.launch[i]].push_back(plan->hp.items[i]);
+  for (size_t i = 0; i < hh.items.size(); ++i)  // keeps the longest-first order inside each launch
+    by_launch[plan->hs.launch[i]].push_back(hh.items[i]);
   std::vector<wa::Item> regrouped;
-  regrouped.reserve(plan->hp.items.size());
+  regrouped.reserve(hh.items.size());
   plan->pc_item_off.assign(n_pieces + 1, 0);
   for (int p = 0; p < n_pieces; ++p) {
     regrouped.insert(regrouped.end(), by_launch[p].begin(), by_launch[p].end());
     plan->pc_item_off[p + 1] = (int)regrouped.size();
   }
   plan->pc_ev.assign(3 * n_pieces + 4, nullptr);
+  const wa::Geometry& g = hh.geo;
+  plan->ws_o_elems_host = (int64_t)g.layout.B * g.layout.H * g.G * hh.n_splits * g.layout.D;
   cudaError_t e = dev_alloc(&plan->d_stage, 4 * span_bytes);
   if (e == cudaSuccess) e = dev_alloc(&plan->d_items_pc, std::max<size_t>(1, regrouped.size()) * sizeof(wa::Item));
+  if (e == cudaSuccess && hh.info.workspace_bytes > 0)
+    e = dev_alloc(&plan->d_ws_host, (size_t)hh.info.workspace_bytes);
   if (e != cudaSuccess) {
     release_host_path(plan);
     return e == cudaErrorMemoryAllocation ? WA_ERR_OOM : WA_ERR_CUDA;
@@ -931,10 +954,10 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
   uint8_t* dst[3] = {dq, dk, dv};
   wa::LaunchArgs a;
   a.q = dq; a.k = dk; a.v = dv; a.out = dout;
-  a.ws_o = plan->d_ws;
-  a.ws_lse = plan->d_ws ? plan->d_ws + plan->ws_o_elems : nullptr;
+  a.ws_o = plan->d_ws_host;
+  a.ws_lse = plan->d_ws_host ? plan->d_ws_host + plan->ws_o_elems_host : nullptr;
   a.err = plan->d_err;
-  a.n_splits = plan->hp.n_splits;
+  a.n_splits = plan->hp_host.n_splits;
   a.debug_flags = 0;
   a.geo = &g;
   for (int p = 0; p < n_pieces; ++p) {

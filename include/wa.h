@@ -146,8 +146,11 @@ wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const 
  * launch completes are copied back while later pieces are still arriving; the global rows of a head range are
  * merged and copied back right after the launch that ran the range's last split items. Launches alternate between `stream` and a library-owned compute stream; copies run on two
  * library-owned copy streams; events chain all of them to `stream`. Other layouts are copied whole and computed in
- * one launch, merged, and copied back whole. Results are identical
- * to wa_forward. The call is asynchronous: out is complete when `stream` reaches this point (e.g. after
+ * one launch, merged, and copied back whole. The work list is the plan's, except that when the global rows fill at
+ * least four query-tile pairs per head the global leg uses key splits half as long (its own workspace, allocated
+ * with the device copies; see wa_host_schedule_describe). Frame rows are identical to wa_forward's bit for bit, and
+ * so are global rows when the two lists split alike; otherwise global rows differ from wa_forward's only in the
+ * order of the split merge (within rounding). The call is asynchronous: out is complete when `stream` reaches this point (e.g. after
  * cudaStreamSynchronize); q, k, v and out must stay valid until then.
  * Errors: WA_ERR_INVALID for null pointers or out overlapping an input; WA_ERR_OOM when the device copies cannot
  * be allocated; WA_ERR_CUDA when a copy or launch fails. Device-side failures: see wa_plan_check_error().
@@ -201,19 +204,25 @@ wa_status wa_geometry_describe(int T, int S, int K, int r, int G, const wa_layou
 
 /*
  * Host-only: the piece schedule wa_forward_host uses for this geometry and layout, without touching any device.
- * Pieces are blocks of sequence rows x heads (all batch entries) in the order they are copied in; after piece p has
- * arrived, launch p runs the work items whose rows have all arrived; after launch p the blocks of out that it
- * completed are copied back: frame rows, and the global rows of the heads whose last split item it ran (merged
- * right behind it). When the pieces are not row blocks, the whole of out is merged and copied back at the end. Writes min(n_pieces, pieces_cap) blocks {lo, hi, h_lo, h_hi} (rows [lo, hi), heads
- * [h_lo, h_hi)) to `pieces`; for each work item, in wa_geometry_describe's order, min(n_items, items_cap) launch
- * indices to `item_launch`; and min(n_out, out_cap) blocks {launch, lo, hi, h_lo, h_hi} to `out_ranges`. Any of
- * the three may be NULL. *n_pieces and *n_out receive the full counts; *row_pieces is 1 when pieces are row blocks
+ * The host-buffer forward runs its own work list: wa_geometry_describe's, except that the key splits of the global
+ * leg are half as long when the global rows fill at least four query-tile pairs per head (a split runs only once
+ * every row of its key range has arrived, so a short last split leaves less work after the last copy); with fewer
+ * global rows the two lists are the same. Pieces are blocks of sequence rows x heads (all batch entries) in the
+ * order they are copied in; after piece p has arrived, launch p runs the work items whose rows have all arrived;
+ * after launch p the blocks of out that it completed are copied back: frame rows, and the global rows of the heads
+ * whose last split item it ran (merged right behind it). When the pieces are not row blocks, the whole of out is
+ * merged and copied back at the end. Writes min(n_pieces, pieces_cap) blocks {lo, hi, h_lo, h_hi} (rows [lo, hi),
+ * heads [h_lo, h_hi)) to `pieces`; for the first min(n_items, items_cap) work items of the host path's list, the
+ * item (8 int64 each, as wa_geometry_describe writes them) to `items` and its launch index to `item_launch`; and
+ * min(n_out, out_cap) blocks {launch, lo, hi, h_lo, h_hi} to `out_ranges`. Any of the four arrays may be NULL.
+ * *n_pieces, *n_items and *n_out receive the full counts; *row_pieces is 1 when pieces are row blocks
  * (stride_h == D or H == 1), else 0 (one piece: the whole tensors).
  * Errors: as wa_plan_create for the arguments, WA_ERR_INVALID for a null count pointer.
  */
 wa_status wa_host_schedule_describe(int T, int S, int K, int r, int G, const wa_layout_t* layout, int64_t* pieces,
-                                    int64_t pieces_cap, int32_t* item_launch, int64_t items_cap, int64_t* out_ranges,
-                                    int64_t out_cap, int64_t* n_pieces, int64_t* n_out, int32_t* row_pieces);
+                                    int64_t pieces_cap, int64_t* items, int32_t* item_launch, int64_t items_cap,
+                                    int64_t* out_ranges, int64_t out_cap, int64_t* n_pieces, int64_t* n_items,
+                                    int64_t* n_out, int32_t* row_pieces);
 
 /* Static string for a status code ("WA_OK", ...); "WA_UNKNOWN" for other values. */
 const char* wa_status_string(wa_status s);

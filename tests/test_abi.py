@@ -103,8 +103,9 @@ def test_item_count_past_int32_is_unsupported(walib, a):
     assert lib.wa_plan_create(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), ctypes.byref(h)) == 2
     assert not h.value
     n = ctypes.c_int64()
-    assert lib.wa_host_schedule_describe(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), None, 0, None, 0,
-                                         None, 0, ctypes.byref(n), ctypes.byref(n), ctypes.byref(ctypes.c_int32())) == 2
+    assert lib.wa_host_schedule_describe(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), None, 0, None,
+                                         None, 0, None, 0, ctypes.byref(n), ctypes.byref(n), ctypes.byref(n),
+                                         ctypes.byref(ctypes.c_int32())) == 2
     p = ctypes.c_void_p(1 << 20)  # never dereferenced: the geometry is rejected first
     assert lib.wa_forward_static(a["T"], a["S"], a["K"], a["r"], a["G"], ctypes.byref(lay), p, p, p,
                                  ctypes.c_void_p(1 << 21), None) == 2

@@ -101,8 +101,34 @@ PIECE_CASES = [
     (configs.Workload("host_one_head_rowpad", B=1, H=1, D=128, T=12, S=33, K=1, r=3, G=7, global_pos=0, seed=69),
      "rowpad"),
     (configs.Workload("host_long_globals", B=1, H=8, D=128, T=40, S=64, K=1, r=0, G=1100, global_pos=0, seed=70),
-     None),  # 2 global splits; the head ranges of the first and last pieces merge their global rows separately
+     None),  # the host path's 2 global splits against the device plan's 1; the head ranges of the first and last
+             # pieces merge their global rows separately
 ]
+
+
+def same_lists(cuda, w, strides):
+    """Whether the host path runs the device plan's work list (it keeps shorter global splits when the global rows
+    are plentiful)."""
+    lay = cuda.make_layout(w.B, w.L, w.H, w.D, w.global_pos, strides)
+    _, _, dev = cuda.wa_geometry_describe(w.T, w.S, w.K, w.r, w.G, lay, with_items=True)
+    return cuda.wa_host_schedule_describe(w.T, w.S, w.K, w.r, w.G, lay)["items"] == dev
+
+
+def check_against_device(cuda, w, got, want, strides):
+    """Bit for bit when the two lists are the same; otherwise the frame rows bit for bit and the global rows (whose
+    split merge differs) within the oracle bar of the parity tests."""
+    if same_lists(cuda, w, strides):
+        assert torch.equal(got, want)
+        return
+    g0 = 0 if w.global_pos else w.T * w.S
+    frames = torch.ones(w.L, dtype=torch.bool)
+    frames[g0:g0 + w.G] = False
+    assert torch.equal(got[:, frames], want[:, frames])
+    for b in range(w.B):
+        for h in range(w.H):
+            a = got[b, g0:g0 + w.G, h].double()
+            r = want[b, g0:g0 + w.G, h].double()
+            assert (a - r).norm() / r.norm() <= 5e-3 and (a - r).abs().max() <= 3e-2
 
 
 @pytest.mark.parametrize("w,kind", PIECE_CASES, ids=[c[0].name for c in PIECE_CASES])
@@ -124,4 +150,4 @@ def test_host_forward_pieces(cuda, w, kind):
         assert plan.check_error() == 0
     finally:
         plan.close()
-    assert torch.equal(got, want)
+    check_against_device(cuda, w, got, want.cpu() if want.is_cuda else want, strides_of(q))

@@ -24,9 +24,9 @@ TILE = 128
 def describe(T, S, K, r, G, B, H, D, global_pos, strides=None):
     L = T * S + G
     layout = wa.make_layout(B, L, H, D, global_pos, strides)
-    info, groups, items = wa.wa_geometry_describe(T, S, K, r, G, layout, with_groups=True, with_items=True)
-    sched = wa.wa_host_schedule_describe(T, S, K, r, G, layout, info["n_items"])
-    return L, info, groups, items, sched
+    info, groups, _ = wa.wa_geometry_describe(T, S, K, r, G, layout, with_groups=True)
+    sched = wa.wa_host_schedule_describe(T, S, K, r, G, layout)
+    return L, info, groups, sched["items"], sched
 
 
 def read_ranges(item, L):
@@ -145,3 +145,28 @@ def test_schedule_caps_the_piece_count():
     L, info, groups, sched = check_schedule(400, 1, 1, 0, 3, 1, 2, 64, 0)
     assert info["n_groups"] == 400
     assert len(sched["pieces"]) == 64
+
+
+def test_host_list_keeps_short_global_splits():
+    # the host-buffer forward's own work list: the plan's window items unchanged, the global leg in key splits half
+    # as long when the global rows are plentiful (H3: 5 splits where the device plan has 3)
+    w = configs.H3
+    layout = wa.make_layout(w.B, w.L, w.H, w.D, w.global_pos)
+    info, _, dev_items = wa.wa_geometry_describe(w.T, w.S, w.K, w.r, w.G, layout, with_items=True)
+    host_items = wa.wa_host_schedule_describe(w.T, w.S, w.K, w.r, w.G, layout)["items"]
+    assert info["n_splits"] == 3
+    assert sorted(i for i in host_items if i[1] == 0) == sorted(i for i in dev_items if i[1] == 0)
+    per_tile = {}
+    for it in host_items:
+        if it[1] == 1:
+            per_tile.setdefault((it[0], it[2]), []).append((it[4], it[5]))
+    assert len(per_tile) == w.H * w.G // 256
+    for segs in per_tile.values():
+        segs.sort()
+        assert len(segs) == 5 and segs[0][0] == 0 and segs[-1][1] == w.L
+        assert all(a[1] == b[0] for a, b in zip(segs, segs[1:]))
+    # with few global rows the two lists are the same
+    m = configs.MEDIUM
+    lay = wa.make_layout(m.B, m.L, m.H, m.D, m.global_pos)
+    _, _, dev_m = wa.wa_geometry_describe(m.T, m.S, m.K, m.r, m.G, lay, with_items=True)
+    assert wa.wa_host_schedule_describe(m.T, m.S, m.K, m.r, m.G, lay)["items"] == dev_m
