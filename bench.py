@@ -383,7 +383,8 @@ def run_backward(args, w):
         "kernel_tflops": {"dq": dq_tf, "dk_dv": dkdv_tf},
         "kernel_frac_of_bf16_peak": {"dq": dq_tf / bf16_peak, "dk_dv": dkdv_tf / bf16_peak},
         "roofline": {"bound": "tensor", "achieved": dkdv_tf, "peak": bf16_peak, "unit": "TFLOP/s",
-                     "frac": dkdv_tf / bf16_peak, "kernel": f"wa_dkdv_kernel<{w.D}>", "kernel_ms": kms[2],
+                     "frac": dkdv_tf / bf16_peak, "frac_of_sustained": dkdv_tf / peaks()[1] if peaks()[1] else None,
+                     "kernel": f"wa_dkdv_kernel<{w.D}>", "kernel_ms": kms[2],
                      "traffic": stored_traffic(BWD_PROFILE_SUMMARY, "wa_backward.cu", "dk/dv dram bytes per full H3 launch")
                      if w.name == "h3" else None},
         "gpu_launches": (3 + (1 if w.G > 0 else 0)) * args.steps, "clocks": clocks}), flush=True)
@@ -612,6 +613,7 @@ def main():
                                                             "kept_tflop_per_step": flops / 1e12}),
                               "roofline": {"bound": "tensor", "achieved": achieved, "peak": mixed_peak,
                                            "unit": "TFLOP/s", "frac": achieved / mixed_peak,
+                                           "frac_of_sustained": achieved / (bf16_sus * 4.0 / 3.0) if bf16_sus else None,
                                            "traffic": stored_traffic(FP8_PROFILE_SUMMARY) if w.name == "h3" else None,
                                            "kernel": f"window_attention_kernel<{w.D}, e4m3>", "kernel_ms": attn_avg,
                                            "merge_kernel_ms": comb_ms / max(1, nrec),
@@ -665,7 +667,8 @@ def main():
                                           "kept_tflop_per_step": flops / 1e12}),
             "pct_of_bf16_peak": 100.0 * value / world / bf16_peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
-                         "frac": achieved / bf16_peak, "traffic": traffic,
+                         "frac": achieved / bf16_peak, "frac_of_sustained": achieved / bf16_sus if bf16_sus else None,
+                         "traffic": traffic,
                          "kernel": f"window_attention_kernel<{w.D}>", "kernel_ms": attn_avg,
                          "merge_kernel_ms": comb_ms / max(1, nrec),
                          "peak_kind": f"{peak_kind} bf16 burst (sustained {bf16_sus})"},
