@@ -145,6 +145,11 @@ unsigned long long current_context_id();
 // attribute belongs to the context, so a second device (or a context rebuilt after a reset) needs its own call.
 // Thread-safe. Returns a CUDA error code (0 on success).
 int ensure_smem_attr(const void* func, int bytes);
+// Capture state of a stream: 0 = not capturing, 1 = being captured into a CUDA graph, -1 = the query failed or the
+// capture was invalidated. A captured call runs whenever the graph is launched, on the stream it is launched on, so
+// it takes no part in a plan's cross-stream ordering: the caller orders graph launches against other uses of the
+// plan (or of the allocation-free entry point's shared array).
+int capture_state(void* stream);
 
 // Encode the 4-D TMA map of a [B, L, H, D] tensor (box 128 bytes x 1 x 128 rows x 1, 128-byte swizzle) into
 // `map` (a 64-byte aligned CUtensorMap). elem_bytes 2: bf16, 1: 8-bit. Returns false if encoding fails.

@@ -102,6 +102,9 @@ extern "C" wa_status wa_forward_static(int T, int S, int K, int r, int G, const 
     cudaGetLastError();
     return WA_ERR_CUDA;
   }
+  cudaStream_t s = (cudaStream_t)stream;
+  const int cap = wa::capture_state(s);
+  if (cap < 0) return WA_ERR_CUDA;
   void* base = nullptr;
   {
     // First call in a context: look up the array's device address with that context current. In host code the
@@ -112,6 +115,7 @@ extern "C" wa_status wa_forward_static(int T, int S, int K, int r, int G, const 
       for (auto& e : g_scratch_addr)
         if (e.first == ctx) base = e.second;
     if (!base) {
+      if (cap) return WA_ERR_UNSUPPORTED;  // the address is looked up by a first call outside a capture
       if (cudaGetSymbolAddress(&base, g_scratch) != cudaSuccess || !base) {
         cudaGetLastError();
         return WA_ERR_CUDA;
@@ -126,7 +130,6 @@ extern "C" wa_status wa_forward_static(int T, int S, int K, int r, int G, const 
   float* ws_o = reinterpret_cast<float*>(b + 256 + items_bytes);
   float* ws_lse = reinterpret_cast<float*>(b + 256 + items_bytes + ws_o_bytes);
 
-  cudaStream_t s = (cudaStream_t)stream;
   // The array keeps the previous call's contents: the first expansion launch clears the error word; the work list
   // is rewritten in full; every workspace entry the merge reads is written by the attention kernel first.
   {

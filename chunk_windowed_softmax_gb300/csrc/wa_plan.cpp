@@ -107,6 +107,16 @@ unsigned long long current_context_id() {
   return id + 1;  // never 0 for a valid context
 }
 
+int capture_state(void* stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing((cudaStream_t)stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (cs == cudaStreamCaptureStatusNone) return 0;
+  return cs == cudaStreamCaptureStatusActive ? 1 : -1;
+}
+
 int ensure_smem_attr(const void* func, int bytes) {
   static std::mutex mu;
   static std::vector<std::pair<const void*, unsigned long long>> done;  // (kernel, context) pairs already set
@@ -507,6 +517,7 @@ constexpr int kMaxProfiled = 4096;
 
 bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) { return a < b + nb && b < a + na; }
 
+
 }  // namespace
 
 extern "C" {
@@ -689,8 +700,10 @@ wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void
     return WA_ERR_INVALID;
   }
   cudaStream_t s = (cudaStream_t)stream;
+  const int cap = wa::capture_state(s);
+  if (cap < 0) return WA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(plan->mu);  // forwards on one plan share its workspace: serialise the host side
-  if (plan->have_last && plan->last_stream != s) {
+  if (!cap && plan->have_last && plan->last_stream != s) {
     if (cudaStreamWaitEvent(s, plan->done, 0) != cudaSuccess) return WA_ERR_CUDA;
   }
   wa::LaunchArgs a;
@@ -708,7 +721,7 @@ wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void
   a.lse = lse;
   a.item_counter = plan->d_counters;
   cudaEvent_t* ev = nullptr;
-  if (plan->profiling && plan->prof_n < kMaxProfiled) {
+  if (!cap && plan->profiling && plan->prof_n < kMaxProfiled) {
     while ((int)plan->prof_ev.size() < 3 * (plan->prof_n + 1)) {
       cudaEvent_t e;
       if (cudaEventCreate(&e) != cudaSuccess) return WA_ERR_CUDA;
@@ -724,6 +737,7 @@ wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void
   if (ev && cudaEventRecord(ev[1], s) != cudaSuccess) return WA_ERR_CUDA;
   if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
   if (ev && cudaEventRecord(ev[2], s) != cudaSuccess) return WA_ERR_CUDA;
+  if (cap) return WA_OK;
   if (cudaEventRecord(plan->done, s) != cudaSuccess) return WA_ERR_CUDA;
   plan->last_stream = s;
   plan->have_last = true;
@@ -779,12 +793,15 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
     return WA_ERR_INVALID;
   }
   cudaStream_t s = (cudaStream_t)stream;
+  const int cap = wa::capture_state(s);
+  if (cap < 0) return WA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(plan->mu);
   const int64_t BH = (int64_t)l.B * l.H;
   const int64_t part = BH * g.G * plan->hp.n_splits * l.D;
   // The partials are written with 16-byte vector stores: start them on a 256-byte boundary after the row dots.
   const int64_t dvec_elems = (BH * g.L + 63) / 64 * 64;
   if (!plan->d_bws) {
+    if (cap) return WA_ERR_UNSUPPORTED;  // the workspace is allocated by a first call outside a capture
     const size_t bytes = (size_t)(dvec_elems + 3 * part) * sizeof(float);
     if (dev_alloc(&plan->d_bws, bytes) != cudaSuccess) {
       cudaGetLastError();
@@ -792,7 +809,7 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
       return WA_ERR_OOM;
     }
   }
-  if (plan->have_last && plan->last_stream != s) {
+  if (!cap && plan->have_last && plan->last_stream != s) {
     if (cudaStreamWaitEvent(s, plan->done, 0) != cudaSuccess) return WA_ERR_CUDA;
   }
   wa::BackwardArgs a;
@@ -809,7 +826,7 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
   a.geo = &g;
   a.item_counter = plan->d_counters;
   void* const* ev = nullptr;
-  if (plan->profiling && plan->bprof_n < kMaxProfiled) {
+  if (!cap && plan->profiling && plan->bprof_n < kMaxProfiled) {
     while ((int)plan->bprof_ev.size() < 5 * (plan->bprof_n + 1)) {
       cudaEvent_t e;
       if (cudaEventCreate(&e) != cudaSuccess) return WA_ERR_CUDA;
@@ -821,6 +838,7 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
     ev = reinterpret_cast<void* const*>(&plan->bprof_ev[5 * plan->bprof_n++]);
   }
   if (wa::launch_backward(a, (void*)s, plan->num_sms, ev) != 0) return WA_ERR_CUDA;
+  if (cap) return WA_OK;
   if (cudaEventRecord(plan->done, s) != cudaSuccess) return WA_ERR_CUDA;
   plan->last_stream = s;
   plan->have_last = true;
@@ -927,6 +945,8 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
     return WA_ERR_INVALID;
   }
   cudaStream_t s = (cudaStream_t)stream;
+  const int cap = wa::capture_state(s);
+  if (cap) return cap > 0 ? WA_ERR_UNSUPPORTED : WA_ERR_CUDA;  // host copies are not captured into graphs
   std::lock_guard<std::mutex> lk(plan->mu);
   const size_t stage_span = (span + 255) / 256 * 256;
   wa_status st = WA_OK;
@@ -1058,6 +1078,8 @@ int wa_plan_profile_read(wa_plan_t* plan, double* attention_ms, double* combine_
 
 wa_status wa_plan_check_error(wa_plan_t* plan, wa_stream_t stream) {
   if (!plan) return WA_ERR_INVALID;
+  const int cap = wa::capture_state(stream);
+  if (cap) return cap > 0 ? WA_ERR_UNSUPPORTED : WA_ERR_CUDA;  // it synchronises: never inside a capture
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return WA_ERR_CUDA;
   int h = 0;
   if (cudaMemcpy(&h, plan->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return WA_ERR_CUDA;

@@ -106,8 +106,15 @@ wa_status wa_plan_create(int T, int S, int K, int r, int G, const wa_layout_t* l
  * device work is two launches (the attention kernel over the plan's work list, then the log-sum-exp merge of
  * the global rows). Forwards on one plan are serialised: a call on a different stream than the previous call
  * first waits for that call to finish on the device, since both use the plan's workspace.
+ * CUDA graphs: a call on a stream that is being captured records the two launches into the graph (their arguments,
+ * including q, k, v and out, are fixed at capture; the plan must outlive the graph). Each launch leaves the plan's
+ * work counter as it found it, so the graph can be replayed any number of times. A captured call takes no part in
+ * the cross-stream ordering above (it runs whenever the graph is launched): the caller must not let a replay run
+ * at the same time as another call on the same plan, captured or not. Make the first call of a process outside a
+ * capture (it sets the kernels' shared-memory attribute).
  * Errors (synchronous, nothing launched): WA_ERR_INVALID for null/misaligned/overlapping pointers;
- * WA_ERR_CUDA when a launch fails. Device-side failures: see wa_plan_check_error().
+ * WA_ERR_CUDA when a launch fails, or when `stream`'s capture state cannot be read or its capture was invalidated.
+ * Device-side failures: see wa_plan_check_error().
  */
 wa_status wa_forward(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out, wa_stream_t stream);
 
@@ -153,7 +160,8 @@ wa_status wa_forward_fp8(wa_plan_t* plan, const void* q8, const void* k8, const 
  * order of the split merge (within rounding). The call is asynchronous: out is complete when `stream` reaches this point (e.g. after
  * cudaStreamSynchronize); q, k, v and out must stay valid until then.
  * Errors: WA_ERR_INVALID for null pointers or out overlapping an input; WA_ERR_OOM when the device copies cannot
- * be allocated; WA_ERR_CUDA when a copy or launch fails. Device-side failures: see wa_plan_check_error().
+ * be allocated; WA_ERR_UNSUPPORTED, nothing queued, while `stream` is being captured into a CUDA graph; WA_ERR_CUDA
+ * when a copy or launch fails. Device-side failures: see wa_plan_check_error().
  */
 wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const void* v, void* out,
                           wa_stream_t stream);
@@ -171,9 +179,10 @@ wa_status wa_forward_host(wa_plan_t* plan, const void* q, const void* k, const v
  *   lse: device fp32 [B][H][L] contiguous, 4-byte aligned.
  * Ordering: as wa_forward (calls on one plan are ordered across streams by the library). The first call on a plan
  * allocates its backward workspace: B*H*L*4 (rounded up to 256) + 3*B*H*G*n_splits*D*4 bytes, kept until the plan is freed.
+ * CUDA graphs: as wa_forward; a call inside a capture needs the workspace of an earlier call outside one.
  * Errors (synchronous, nothing launched): WA_ERR_INVALID for null or misaligned pointers, or when dq, dk or dv
- * overlaps each other or any input; WA_ERR_OOM when the workspace cannot be allocated; WA_ERR_CUDA when a launch
- * fails. Device-side failures: see wa_plan_check_error(); besides the wait watchdog, the dk/dv kernel at D = 128
+ * overlaps each other or any input; WA_ERR_OOM when the workspace cannot be allocated; WA_ERR_UNSUPPORTED for a
+ * first call made inside a capture; WA_ERR_CUDA when a launch fails. Device-side failures: see wa_plan_check_error(); besides the wait watchdog, the dk/dv kernel at D = 128
  * reports WA_ERR_DEVICE_BOUNDS (and computes nothing) if the device gives it a dynamic shared-memory window more
  * than 768 bytes short of a 1024-byte boundary, since its buffers leave only that much room to realign it (any
  * window on a 256-byte boundary is fine).
@@ -183,7 +192,9 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
 
 /*
  * Synchronise `stream`, then read and clear the plan's device error word.
- * Returns WA_OK, WA_ERR_DEVICE_TIMEOUT, WA_ERR_DEVICE_BOUNDS, or WA_ERR_CUDA if the synchronisation failed.
+ * Returns WA_OK, WA_ERR_DEVICE_TIMEOUT, WA_ERR_DEVICE_BOUNDS, or WA_ERR_CUDA if the synchronisation failed;
+ * WA_ERR_UNSUPPORTED, touching nothing, while `stream` is being captured into a CUDA graph (call it after the
+ * graph's launch instead).
  */
 wa_status wa_plan_check_error(wa_plan_t* plan, wa_stream_t stream);
 
@@ -241,7 +252,8 @@ const char* wa_status_string(wa_status s);
  *   read by the device after the call returns.
  *   The first call in a CUDA context (the device's primary context, or a new one after cudaDeviceReset) looks up
  *   the array's device address (cudaGetSymbolAddress) with that context current; make that first call before any
- *   stream capture.
+ *   stream capture (inside a capture it returns WA_ERR_UNSUPPORTED). Later calls can be captured into a CUDA graph:
+ *   the work list travels in the launches' parameters, so a replay reads nothing from the host.
  *   Every call shares the one array: calls that overlap on the GPU (different streams or threads) race on it;
  *   calls on one stream are ordered. The array keeps the previous call's contents; the call clears what must
  *   start at zero.

@@ -94,3 +94,31 @@ def test_dynamic_claiming_matches_static_striding(cuda):
                 assert torch.equal(out, static_forward(cuda, w, q, k, v))
         finally:
             plan.close()
+
+
+def test_static_forward_in_a_cuda_graph(cuda):
+    """After a first call in the context (it looks up the array's address), the allocation-free forward can be
+    captured: the work list travels in the launches' parameters, so every replay rewrites it on the device and
+    reads nothing from the host. Two replays on fresh inputs equal eager calls bit for bit (MANY_GROUPS: two
+    expansion launches per call)."""
+    w = MANY_GROUPS
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    static_forward(cuda, w, q, k, v)
+    out = torch.empty_like(q)
+    lay = cuda.make_layout(w.B, w.L, w.H, w.D, w.global_pos)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        s = torch.cuda.current_stream().cuda_stream
+        st = cuda.lib().wa_forward_static(w.T, w.S, w.K, w.r, w.G, ctypes.byref(lay), ctypes.c_void_p(q.data_ptr()),
+                                          ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+                                          ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(s))
+    assert st == 0, cuda.wa_status_string(st)
+    for seed in (31, 32):
+        q2, k2, v2 = inputs.make_qkv(w, seed=seed, device="cuda")
+        q.copy_(q2)
+        k.copy_(k2)
+        v.copy_(v2)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, static_forward(cuda, w, q2, k2, v2)), f"seed {seed}"
