@@ -56,6 +56,27 @@ def compare(got, want, label):
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_alternating_items_bf16_and_lse(cuda, w):
     q, k, v = inputs.make_qkv(w, device="cuda")
+    check_bf16_and_lse(cuda, w, q, k, v)
+
+
+# Hot scores: q and k times 4 (exact in bf16), so the scores' standard deviation is 16 and the lazy reference max
+# is raised again and again: in pair items, in both halves of alternating items (whose halves then merge across
+# very different references) and in the global splits.
+HOT = configs.Workload("alt_hot", B=1, H=4, D=128, T=10, S=150, K=2, r=1, G=200, global_pos=0, seed=84)
+
+
+def test_hot_case_holds_alternating_items(walib):
+    assert {k[0] for k in describe_kinds(walib, HOT)} >= {"pair", "alternating"}
+
+
+@pytest.mark.gpu
+def test_hot_scores_bf16_and_lse(cuda):
+    w = HOT
+    q, k, v = inputs.make_qkv(w, device="cuda")
+    check_bf16_and_lse(cuda, w, q * 4, k * 4, v)
+
+
+def check_bf16_and_lse(cuda, w, q, k, v):
     plan = cuda.Plan(w.T, w.S, w.K, w.r, w.G, w.B, w.H, w.D, w.global_pos)
     try:
         out, lse = plan.forward_lse(q, k, v)
