@@ -58,6 +58,35 @@ def test_forward_graph_replays_equal_eager_calls(cuda):
         plan.close()
 
 
+def test_fp8_forward_graph(cuda):
+    """The e4m3 forward (scales fixed at capture, as every launch argument is) replays like its eager call."""
+    w = W
+    plan = new_plan(cuda, w)
+    try:
+        q, k, v = inputs.make_qkv(w, device="cuda")
+        sq, sk = 8.0 / 448.0, 8.0 / 448.0  # N(0, 1) draws stay below 8: nothing leaves the e4m3 range
+        q8, k8 = (q.float() / sq).to(torch.float8_e4m3fn), (k.float() / sk).to(torch.float8_e4m3fn)
+        out = torch.empty_like(v)
+        plan.forward_fp8(q8, k8, v, sq, sk, out=out)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.forward_fp8(q8, k8, v, sq, sk, out=out)
+        for seed in (121, 122):
+            q2, k2, v2 = inputs.make_qkv(w, seed=seed, device="cuda")
+            q8.copy_((q2.float() / sq).to(torch.float8_e4m3fn))
+            k8.copy_((k2.float() / sk).to(torch.float8_e4m3fn))
+            v.copy_(v2)
+            out.fill_(float("nan"))
+            g.replay()
+            want = plan.forward_fp8(q8.clone(), k8.clone(), v2, sq, sk)
+            torch.cuda.synchronize()
+            assert torch.equal(out, want), f"seed {seed}"
+        assert plan.check_error() == 0
+    finally:
+        plan.close()
+
+
 def test_forward_lse_and_backward_graph(cuda):
     w = W
     plan = new_plan(cuda, w)
