@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           uint32_t dpr[kCW / 32][32];
 #pragma unroll
-          for (int ch = 0; ch < kCW / 32; ++ch) tmem_ld_x32(tR2 + lane_base + col0 + 32 * ch, dpr[ch]);
+          tmem_ld_x64(tR2 + lane_base + col0, *reinterpret_cast<uint32_t(*)[kCW]>(&dpr[0][0]));  // one wait
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(b_dpfree);
@@ -872,10 +872,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t cb = sCol + ds * C::kColBytes + col0 * 4;  // -lse' of this thread's first column
           // Phase A: P^T = 2^(s c' - lse'_col) over this thread's query columns
           float p[kCW];
+          uint32_t sr64[kCW];  // this thread's score columns in one TMEM load (one wait, not one per 32 columns)
+          tmem_ld_x64(tS + lane_base + col0, sr64);
 #pragma unroll
           for (int ch = 0; ch < kCW / 32; ++ch) {
-            uint32_t sr[32], pk[16];
-            tmem_ld_x32(tS + lane_base + col0 + 32 * ch, sr);
+            uint32_t pk[16];
+            const uint32_t* sr = sr64 + 32 * ch;
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
               const float4 nl = lds_f4(cb + (32 * ch + 4 * c4) * 4);  // -lse' of 4 columns
@@ -904,10 +906,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           s_n++;
           if (!ok) break;
           tc_fence_after();
+          uint32_t dr64[kCW];  // this thread's dP^T columns in one TMEM load
+          tmem_ld_x64(tDP + lane_base + col0, dr64);
 #pragma unroll
           for (int ch = 0; ch < kCW / 32; ++ch) {
-            uint32_t dr[32], pk[16];
-            tmem_ld_x32(tDP + lane_base + col0 + 32 * ch, dr);
+            uint32_t pk[16];
+            const uint32_t* dr = dr64 + 32 * ch;
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
               const float4 nd = lds_f4(cb + 512 + (32 * ch + 4 * c4) * 4);  // -Dvec of 4 columns
