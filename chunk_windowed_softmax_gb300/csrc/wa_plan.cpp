@@ -737,7 +737,7 @@ wa_status forward_impl(wa_plan_t* plan, const void* q, const void* k, const void
   if (ev && cudaEventRecord(ev[1], s) != cudaSuccess) return WA_ERR_CUDA;
   if (g.G > 0 && wa::launch_combine(a, (void*)s) != 0) return WA_ERR_CUDA;
   if (ev && cudaEventRecord(ev[2], s) != cudaSuccess) return WA_ERR_CUDA;
-  if (cap) return WA_OK;
+  if (cap) return WA_OK;  // captured: the graph's launches are ordered by the stream the graph is launched on
   if (cudaEventRecord(plan->done, s) != cudaSuccess) return WA_ERR_CUDA;
   plan->last_stream = s;
   plan->have_last = true;
@@ -838,7 +838,7 @@ wa_status wa_backward(wa_plan_t* plan, const void* q, const void* k, const void*
     ev = reinterpret_cast<void* const*>(&plan->bprof_ev[5 * plan->bprof_n++]);
   }
   if (wa::launch_backward(a, (void*)s, plan->num_sms, ev) != 0) return WA_ERR_CUDA;
-  if (cap) return WA_OK;
+  if (cap) return WA_OK;  // captured: as in the forward, no cross-stream bookkeeping
   if (cudaEventRecord(plan->done, s) != cudaSuccess) return WA_ERR_CUDA;
   plan->last_stream = s;
   plan->have_last = true;
